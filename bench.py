@@ -1,0 +1,381 @@
+"""Benchmark: forward + backward exact attention on one batch per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mid_n4096_d128] [--no-cpu-baseline] [--no-e2e]
+
+A step is one pass of the whole hot path over one batch: fa_fwd (one kernel)
+then fa_bwd (pre, main, post kernels).  Inputs are seeded synthetic bf16
+tensors already resident in device memory; L2 is flushed (a 256 MiB write)
+between timed steps, outside the per-step CUDA events.  FLOPs follow the
+usual convention: forward 4·B·H·N²·d, backward 2.5x, both halved when causal.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU with
+no collective on the data path (weak scaling); timing uses a barrier and the
+maximum over ranks, and rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (the reference definition) on the
+host cores, on a bounded sample of the same workload (whole (batch, head)
+problems), with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from io_aware_attention_flash_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fwd/bwd attention TFLOP/s and % of GB300 BF16 tensor peak, N=4096 d=128"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("hbm_gbs", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _workload_desc(w: wl.Workload) -> str:
+    return f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {'causal' if w.causal else 'non-causal'}"
+
+
+def _host_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def time_oracle_sample(w: wl.Workload, budget_s: float, seed: int = 0):
+    """Run the fp64 oracle forward + backward on whole (batch, head) problems
+    of the workload until `budget_s` has elapsed (at least one).  Returns
+    (TFLOP/s by the workload's FLOP convention, seconds, heads done)."""
+    import numpy as np
+
+    import oracle
+
+    q, k, v, do = wl.workload_inputs(w, seed)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
+        qd, kd, vd, dod = (t[sl].float().double().numpy() for t in (q, k, v, do))
+        oracle.forward(qd, kd, vd, w.scale, w.causal)
+        oracle.backward(qd, kd, vd, dod, w.scale, w.causal)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = (wl.flops_fwd(1, w.d, [w.N], w.causal) + wl.flops_bwd(1, w.d, [w.N], w.causal)) * done
+    del np
+    return flops / dt / 1e12, dt, done
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        time_oracle_sample(w, 0.0)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, dt, _ = time_oracle_sample(w, 0.0)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.mean(vals)
+    cores = _host_cores()
+    sample = f"one (batch, head) problem of {w.name} per step (fwd+bwd, fp64 numpy oracle), {_cpu_model()}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+        return False
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_gpu(args, w):
+    import io_aware_attention_flash_gb300 as fa
+    from io_aware_attention_flash_gb300 import build as fabuild
+
+    ws_n, rank, local = _dist()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws_n == 1:
+        fabuild.build()
+    if ws_n > 1:
+        dist.barrier()
+    fa.load_library()
+
+    def barrier():
+        if ws_n > 1:
+            dist.barrier()
+
+    # Inputs for this rank: every rank draws its own batch (seed + rank).
+    q_h, k_h, v_h, do_h = wl.workload_inputs(w, seed=args.seed + rank)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    f_fwd = wl.flops_fwd(w.H, w.d, [w.N] * w.B, w.causal)
+    f_bwd = wl.flops_bwd(w.H, w.d, [w.N] * w.B, w.causal)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, w.causal)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, wsp, w.causal)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(K):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, w.causal)
+            e[1].record(stream)
+            fa.fa_set_kernel_events(e[2], e[3])
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, wsp, w.causal)
+            e[4].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e = None
+        if not args.no_e2e:
+            e2e = run_e2e(fa, w, dev, stream, (q_h, k_h, v_h, do_h), K, flush)
+    if fa.fa_get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
+    main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = statistics.mean(step_ms)
+    t = torch.tensor([t_step, statistics.mean(fwd_ms), statistics.mean(bwd_ms), statistics.mean(main_ms)],
+                     device=dev, dtype=torch.float64)
+    if ws_n > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_step, t_fwd, t_bwd, t_main = t.tolist()
+    if e2e is not None and ws_n > 1:
+        te = torch.tensor([e2e["ms"]], device=dev, dtype=torch.float64)
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e["ms"] = te.item()
+
+    peak, hbm_peak, peak_kind = _peaks()
+    value = ws_n * (f_fwd + f_bwd) / (t_step * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (t_fwd * 1e-3) / 1e12
+    bwd_tflops = f_bwd / (t_bwd * 1e-3) / 1e12
+    # Dominant kernel: the backward main kernel carries all backward FLOPs.
+    main_tflops = f_bwd / (t_main * 1e-3) / 1e12
+    traffic = _committed_traffic(w.name, "fa_bwd_main")
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "seed": args.seed, "l2": "flushed: 256 MiB write between steps, outside the step events",
+                   "parallelism": f"weak x{ws_n} (independent batch per GPU)"},
+        "fwd": {"ms": t_fwd, "tflops": fwd_tflops, "frac_of_peak": fwd_tflops / peak},
+        "bwd": {"ms": t_bwd, "tflops": bwd_tflops, "frac_of_peak": bwd_tflops / peak, "main_kernel_ms": t_main},
+        "roofline": {"kernel": "fa_bwd_main_kernel", "bound": "tensor", "achieved": main_tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": main_tflops / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 1.9 PFLOP/s bf16"},
+        "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        result["e2e"] = {"value": ws_n * (f_fwd + f_bwd) / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"]}
+    if rank == 0 and not args.no_cpu_baseline and ws_n == 1:
+        v_cpu, dt, heads = time_oracle_sample(w, args.cpu_budget)
+        result["cpu_baseline"] = {
+            "value": v_cpu, "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} (batch, head) problems of {w.name}, fwd+bwd, fp64 numpy oracle, "
+                      f"{dt:.1f} s on {_cpu_model()}"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws_n > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
+    """Same step through the public API with pinned host buffers: the inputs
+    go host->device and O, LSE, dQ, dK, dV come back, inside the timed region."""
+    hq, hk, hv, hdo = (t.pin_memory() for t in host_inputs)
+    q, k, v, do = (torch.empty_like(t, device=dev) for t in host_inputs)
+    outs_h = [torch.empty_like(hq).pin_memory() for _ in range(4)]
+    lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h) + lse_h.numel() * 4
+    wsp = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+    times = []
+    for i in range(K + 2):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            dst.copy_(src, non_blocking=True)
+        o, lse = fa.attention_forward(q, k, v, w.causal)
+        dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, w.causal, workspace=wsp)
+        for dst, src in zip(outs_h, (o, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    return {"ms": statistics.mean(times), "h2d": h2d, "d2h": d2h}
+
+
+def _committed_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one
+    exists for this workload (profiles/<kernel>__<workload>.json)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mid_n4096_d128", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = wl.WORKLOADS[args.workload]
+    if w.varlen:
+        ap.error("the benchmark times dense workloads; varlen is covered by the tests")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

@@ -1,0 +1,173 @@
+/*
+ * fa.h — C ABI of libfa_gb300: exact IO-aware softmax attention on GB300
+ * (sm_103a), forward and backward, dense batches and packed variable-length
+ * batches.
+ *
+ * Operation (all entry points):
+ *   S = scale · Q Kᵀ, P = softmax(S) row by row, O = P V
+ *   ("08 · FlashAttention", section 一; "LLM Systems 22: Flash Attention",
+ *   section 2.1).  The forward never forms S or P in device memory: it streams
+ *   K/V tiles through shared memory and keeps a running row max m and row sum
+ *   l, rescaling the partial O as m grows ("LLM Systems 22", section 3.1;
+ *   "08 · FlashAttention", section 二), and writes O and the row log-sum-exp
+ *   only.  The backward recomputes P tile by tile from Q, K and the saved LSE
+ *   ("LLM Systems 22", section 3.2; "08 · FlashAttention", section 三) and
+ *   forms dV = Pᵀ dO, dP = dO Vᵀ, dS = P ∘ (dP − D), dQ = scale · dS K,
+ *   dK = scale · dSᵀ Q with D_i = Σ_k dO_ik O_ik.
+ *
+ * Conventions shared by every entry point:
+ *   - Element type: bf16 for q, k, v, o, do, dq, dk, dv (raw 16-bit words),
+ *     fp32 for lse and the workspace.
+ *   - Dense layout [B, N, H, d], row-major: element (b, n, h, k) at
+ *     ((b·N + n)·H + h)·d + k — the token-major layout of the ``mha_fwd``
+ *     entry in "Flash Attention实现深度解析" (seekfood), section 3.1.
+ *     Packed layout [T, H, d]: sequence s occupies rows
+ *     cu_seqlens[s] .. cu_seqlens[s+1]−1.
+ *   - LSE: fp32 [B, H, N] (packed: [nseq, H, max_seqlen]); natural log of the
+ *     scaled scores, LSE_i = ln Σ_j exp(S_ij) over visible keys.  Entries
+ *     past a packed sequence's length are not written.
+ *   - causal != 0: key j is visible to query i iff j <= i (within a sequence);
+ *     no other masks are supported ("08 · FlashAttention", section 四).
+ *   - d must be 64 or 128.  Every pointer must be a device pointer, 16-byte
+ *     aligned, all on one device; the call makes the device owning q current
+ *     on the calling thread and launches there.  The caller owns every
+ *     buffer; the library allocates nothing and never frees.  All work is
+ *     enqueued on `stream` (a cudaStream_t of that device; NULL = legacy
+ *     default stream) and returns without synchronising.
+ *   - Errors: argument errors are detected on the host before any launch and
+ *     returned as a non-zero fa_status; nothing is enqueued then.  There is
+ *     no fallback path: an unsupported case is an error, never a slower
+ *     route.  Device-side failures (a bounded wait that ran out) are reported
+ *     by fa_get_device_error().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+typedef int fa_status;
+
+enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,          /* a required pointer is NULL */
+  FA_ERR_ALIGN = 2,         /* a pointer is not 16-byte aligned */
+  FA_ERR_HEAD_DIM = 3,      /* d not in {64, 128} */
+  FA_ERR_SHAPE = 4,         /* B, H, N, nseq, total or max_seqlen out of range */
+  FA_ERR_ARCH = 5,          /* current device is not compute capability 10.3 */
+  FA_ERR_CUDA = 6,          /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 7,       /* a kernel's bounded wait expired (device side) */
+  FA_ERR_WORKSPACE = 8,     /* workspace missing or smaller than required */
+  FA_ERR_SCALE = 9,         /* scale not finite */
+  FA_ERR_NOT_DEVICE = 10    /* q is not device memory (its device is the one launched on) */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+FA_API const char* fa_status_string(fa_status status);
+
+/*
+ * Forward, dense batch.
+ *   q, k, v  [in]  bf16 [B, N, H, d]
+ *   o        [out] bf16 [B, N, H, d]
+ *   lse      [out] fp32 [B, H, N]
+ *   scale    softmax scale applied to Q Kᵀ (usually 1/sqrt(d))
+ * Tiling with online softmax: "LLM Systems 22", section 3.1 and
+ * "08 · FlashAttention", section 二 (query tile outer, key/value tiles inner,
+ * O written once).
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, void* stream);
+
+/* Bytes of fp32 workspace fa_bwd needs: D [B, H, N] and the dQ accumulator
+ * [B, N, H, d], each padded to 256 bytes. */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward, dense batch.  Recomputes P from q, k and lse ("LLM Systems 22",
+ * section 3.2: keep only the row statistics, reload Q, K, V tile by tile and
+ * rebuild the attention tile on chip).
+ *   q, k, v, o, dout [in]  bf16 [B, N, H, d] (o and lse from fa_fwd)
+ *   lse              [in]  fp32 [B, H, N]
+ *   dq, dk, dv       [out] bf16 [B, N, H, d]
+ *   workspace        device scratch of at least fa_bwd_workspace_bytes(),
+ *                    16-byte aligned; contents on entry are ignored.
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, void* stream);
+
+/*
+ * Forward, packed variable-length batch ("08 · FlashAttention", section 四:
+ * packing with cu_seqlens instead of a padding mask).
+ *   q, k, v     [in]  bf16 [total, H, d]
+ *   o           [out] bf16 [total, H, d]
+ *   lse         [out] fp32 [nseq, H, max_seqlen]
+ *   cu_seqlens  [in]  device int32 [nseq + 1], cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[nseq] = total, every length <= max_seqlen.  The
+ *               library does not read it on the host; a violation is
+ *               undefined behaviour (out-of-range rows are not touched, but
+ *               results are meaningless).
+ */
+FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                        int nseq, int max_seqlen, int total, int H, int d, float scale, int causal, void* stream);
+
+/* Workspace for fa_bwd_varlen: D [nseq, H, max_seqlen] and the dQ
+ * accumulator [total, H, d], fp32, each padded to 256 bytes. */
+FA_API size_t fa_bwd_varlen_workspace_bytes(int total, int nseq, int max_seqlen, int H, int d);
+
+/* Backward, packed variable-length batch; arguments as fa_bwd and
+ * fa_fwd_varlen. */
+FA_API fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        const int* cu_seqlens, int nseq, int max_seqlen, int total, int H, int d, float scale,
+                        int causal, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns FA_OK, FA_ERR_TIMEOUT (some kernel's bounded mbarrier wait
+ * ran out and the kernel returned early: its outputs are invalid) or
+ * FA_ERR_CUDA (the synchronisation itself failed).
+ */
+FA_API fa_status fa_get_device_error(void* stream);
+
+/* Text describing the most recent FA_ERR_CUDA returned on the calling host
+ * thread (which call failed and the CUDA error string); "" if none.  The
+ * string is owned by the library and valid until the next call on this
+ * thread. */
+FA_API const char* fa_last_error_detail(void);
+
+/*
+ * Self-test of the bounded-wait path (no counterpart on the pages): launches
+ * one CTA that waits on an mbarrier nothing ever arrives on, with a limit of
+ * `limit_ns` nanoseconds (clamped to [1e3, 2e9]).  The kernel gives up after
+ * the limit, records FA_ERR_TIMEOUT in the error word and exits normally, so
+ * fa_get_device_error() afterwards returns FA_ERR_TIMEOUT.
+ */
+FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/*
+ * Kernel timing hook (no counterpart on the pages; for measurement only).
+ * Makes the next fa_bwd / fa_bwd_varlen call issued from this host thread
+ * record `start_event` immediately before and `end_event` immediately after
+ * its main kernel (the tile loop), on that call's stream, so the caller can
+ * time that kernel alone with cudaEventElapsedTime.  Both are cudaEvent_t
+ * handles created by the caller; the hook is consumed by that one call.
+ * Passing NULL for both clears a pending hook.
+ */
+FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

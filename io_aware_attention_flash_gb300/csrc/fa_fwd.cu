@@ -1,0 +1,400 @@
+// Forward attention kernel for sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (sequence, head) and streams the
+// 128-key K/V tiles of that head through shared memory (query tile outer,
+// key/value tile inner, O written once: "08 · FlashAttention", section 二).
+// Warp roles:
+//   warps 0-3, 4-7  softmax warpgroups, one per query tile; thread r of a
+//                   warpgroup owns query row r (TMEM lane r), so row max and
+//                   row sum need no shuffles.
+//   warp 8          TMA producer (Q once, K/V through multi-stage rings).
+//   warp 9          tcgen05.mma issuer.
+// Per key tile j and query tile t:
+//   S_t = Q_t K_jᵀ                    SMEM x SMEM -> TMEM (fp32, 128 cols)
+//   softmax t: m, P = 2^(c·S − c·m_ref), l += Σ P, P as bf16 over S in TMEM
+//   O_t += P_t V_j                    TMEM(A) x SMEM -> TMEM (fp32, d cols)
+// The MMA order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) lets softmax of one
+// query tile run while the tensor core works on the other ("LLM Systems 22",
+// sections 4.1.2 and 4.2.1: overlap of GEMM and exponentials across tiles).
+//
+// Online softmax ("LLM Systems 22", section 3.1; "08 · FlashAttention",
+// section 二) with the scale folded into the base-2 exponent
+// (c = scale·log2 e) and the output kept unnormalised until the end.  The
+// reference max m_ref is only moved when the tile max exceeds it by more than
+// 2^8 in exponent terms; otherwise P may exceed 1 (by at most 256) and the
+// rescale of O in TMEM is skipped ("LLM Systems 22", section 4.2.1: an online
+// softmax variant that skips most rescaling).  The result is exact after the
+// final division by l.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "fa_kernels.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NQT = 2;                         // query tiles per CTA
+  static constexpr int KB = D / 64;                     // 128-byte swizzle blocks per row
+  static constexpr int BLK_BYTES = kTile * 128;         // one 128-row x 64-col block
+  static constexpr int TILE_BYTES = KB * BLK_BYTES;     // one 128 x D tile
+  static constexpr int NSK = (D == 128) ? 3 : 4;        // K ring depth
+  static constexpr int NSV = (D == 128) ? 2 : 4;        // V ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQT * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
+  // barriers: q, kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT], odone, drain
+  static constexpr int B_Q = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + NSK;
+  static constexpr int B_VFULL = B_KEMPTY + NSK;
+  static constexpr int B_VEMPTY = B_VFULL + NSV;
+  static constexpr int B_SFULL = B_VEMPTY + NSV;
+  static constexpr int B_PFULL = B_SFULL + NQT;
+  static constexpr int B_ODONE = B_PFULL + NQT;
+  static constexpr int B_DRAIN = B_ODONE + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack to align the base to 1024
+  static constexpr int NUM_WARPS = 4 * NQT + 2;
+  static constexpr int NUM_THREADS = NUM_WARPS * 32;
+  static constexpr int PRODUCER_WARP = 4 * NQT;
+  static constexpr int MMA_WARP = 4 * NQT + 1;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns: S_t (P_t aliases its first 64 columns) and O_t.
+  __host__ __device__ static constexpr uint32_t S_COL(int t) { return t * 128; }
+  __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256 + t * D; }
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int NQT = C::NQT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_base + pad;
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SeqPos sp = seq_pos(p.sv);
+  const int ctile = p.causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  const int q0 = ctile * kTile * NQT;
+  if (q0 >= sp.seqlen) return;  // whole CTA past the end of a short packed sequence
+
+  const int nkv_total = (sp.seqlen + kTile - 1) / kTile;
+  int nkv[NQT];
+  int nkv_max = 0;
+#pragma unroll
+  for (int t = 0; t < NQT; ++t) {
+    const int qt = q0 + t * kTile;
+    nkv[t] = qt >= sp.seqlen ? 0 : (p.causal ? min(nkv_total, qt / kTile + 1) : nkv_total);
+    nkv_max = max(nkv_max, nkv[t]);
+  }
+
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::NSK; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
+      mbar_init(bar(C::B_VFULL + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(bar(C::B_SFULL + t), 1);
+      mbar_init(bar(C::B_PFULL + t), 128);
+    }
+    mbar_init(bar(C::B_ODONE), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::PRODUCER_WARP) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t qbytes = 0;
+      for (int t = 0; t < NQT; ++t)
+        if (nkv[t] > 0) qbytes += C::TILE_BYTES;
+      mbar_arrive_expect_tx(bar(C::B_Q), qbytes);
+      for (int t = 0; t < NQT; ++t) {
+        if (nkv[t] == 0) continue;
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_4d(sb + C::OFF_Q + t * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_Q), kb * 64, sp.h,
+                      sp.tma_row0 + q0 + t * kTile, sp.tma_b);
+      }
+      int k_fills = 0, v_fills = 0;
+      for (int j = 0; j < nkv_max; ++j) {
+        const int ks = j % C::NSK;
+        if (j >= C::NSK && !wait_bounded(bar(C::B_KEMPTY + ks), ((j / C::NSK) - 1) & 1, abort_flag, p.err,
+                                         p.timeout_ns))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + kb * C::BLK_BYTES, &tmK, bar(C::B_KFULL + ks),
+                      kb * 64, sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+        ++k_fills;
+        const int vs = j % C::NSV;
+        if (j >= C::NSV && !wait_bounded(bar(C::B_VEMPTY + vs), ((j / C::NSV) - 1) & 1, abort_flag, p.err,
+                                         p.timeout_ns))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmV, bar(C::B_VFULL + vs),
+                      kb * 64, sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+        ++v_fills;
+      }
+      if (*abort_flag) {
+        // Unwinding: let every copy already issued land before the CTA exits.
+        wait_drain(bar(C::B_Q), 0, p.err, p.timeout_ns);
+        for (int s = 0; s < C::NSK && s < k_fills; ++s)
+          wait_drain(bar(C::B_KFULL + s), ((s + ((k_fills - 1 - s) / C::NSK) * C::NSK) / C::NSK) & 1, p.err,
+                     p.timeout_ns);
+        for (int s = 0; s < C::NSV && s < v_fills; ++s)
+          wait_drain(bar(C::B_VFULL + s), ((s + ((v_fills - 1 - s) / C::NSV) * C::NSV) / C::NSV) & 1, p.err,
+                     p.timeout_ns);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int t, int ks) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
+          const uint64_t a = sdesc_sw128(sb + C::OFF_Q + t * C::TILE_BYTES + koff, 16, 1024);
+          const uint64_t b = sdesc_sw128(sb + C::OFF_K + ks * C::TILE_BYTES + koff, 16, 1024);
+          mma_ss(tmem + C::S_COL(t), a, b, idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int vs, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(sb + C::OFF_V + vs * C::TILE_BYTES + kk * 2048, C::BLK_BYTES, 1024);
+          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bounded(bar(C::B_Q), 0, abort_flag, p.err, p.timeout_ns) &&
+                wait_bounded(bar(C::B_KFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NQT; ++t) {
+          if (nkv[t] > 0) {
+            issue_s(t, 0);
+            tc_commit(bar(C::B_SFULL + t));
+          }
+        }
+        tc_commit(bar(C::B_KEMPTY + 0));
+      }
+      for (int j = 0; ok && j < nkv_max; ++j) {
+        const int vs = j % C::NSV;
+        const bool next = j + 1 < nkv_max;
+        const int ks1 = (j + 1) % C::NSK;
+        ok = wait_bounded(bar(C::B_VFULL + vs), (j / C::NSV) & 1, abort_flag, p.err, p.timeout_ns);
+        if (ok && next) ok = wait_bounded(bar(C::B_KFULL + ks1), ((j + 1) / C::NSK) & 1, abort_flag, p.err,
+                                          p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (j < nkv[t]) {
+            if (!wait_bounded(bar(C::B_PFULL + t), j & 1, abort_flag, p.err, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, vs, j > 0);
+          }
+          if (j + 1 < nkv[t]) {
+            issue_s(t, ks1);
+            tc_commit(bar(C::B_SFULL + t));
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar(C::B_VEMPTY + vs));
+        if (next) tc_commit(bar(C::B_KEMPTY + ks1));
+      }
+      if (ok) tc_commit(bar(C::B_ODONE));
+      // Every MMA issued so far must finish before TMEM is released.
+      tc_commit(bar(C::B_DRAIN));
+      wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int t = warp / 4;
+    const int wq = warp % 4;
+    const int r = wq * 32 + lane;
+    const int qt = q0 + t * kTile;
+    const int q_row = qt + r;  // row within the sequence
+    if (nkv[t] > 0) {
+      const float c = p.scale_log2;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+      const uint32_t tS = lane_addr + C::S_COL(t);
+      const uint32_t tO = lane_addr + C::O_COL(t);
+      float m_ref = -CUDART_INF_F;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkv[t]; ++j) {
+        if (!wait_bounded(bar(C::B_SFULL + t), j & 1, abort_flag, p.err, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(tS + ch * 32, s[ch]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) reg_fence(s[ch]);
+
+        const int kv0 = j * kTile;
+        const bool need_mask = (kv0 + kTile > sp.seqlen) || (p.causal && kv0 + kTile - 1 > qt);
+        if (need_mask) {
+          const int lim = p.causal ? min(sp.seqlen - 1, q_row) : sp.seqlen - 1;  // last visible key
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kv0 + ch * 32 + i > lim) s[ch][i] = __float_as_uint(-CUDART_INF_F);
+        }
+        float mt = -CUDART_INF_F;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(s[ch][i]));
+
+        if (j == 0) {
+          m_ref = mt;
+        } else {
+          const bool need = (mt - m_ref) * c > 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx((m_ref - mt) * c) : 1.0f;
+            if (need) {
+              m_ref = mt;
+              l *= alpha;
+            }
+            // 16 columns at a time: the 128 S values of the row stay live here.
+#pragma unroll 1
+            for (int ch = 0; ch < D / 16; ++ch) {
+              uint32_t o[16];
+              tmem_ld16(tO + ch * 16, o);
+              tmem_wait_ld();
+              reg_fence(o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(tO + ch * 16, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        const float mc = (m_ref == -CUDART_INF_F) ? 0.f : m_ref * c;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e]), c, -mc));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e + 1]), c, -mc));
+            l += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + ch * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PFULL + t));
+      }
+      if (ok) ok = wait_bounded(bar(C::B_ODONE), 0, abort_flag, p.err, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const bool store = q_row < sp.seqlen;
+        uint16_t* orow = p.o + (static_cast<size_t>(sp.row_base + q_row) * p.sv.H + sp.h) * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + ch * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+              dst[v4] = w;
+            }
+          }
+        }
+        if (store) {
+          const float lse = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -CUDART_INF_F;
+          p.lse[(static_cast<size_t>(sp.bs) * p.sv.H + sp.h) * p.sv.lse_stride + q_row] = lse;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                         int nseq, int max_seqlen, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  static bool configured = false;  // per process; attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(nseq * p.sv.H, (max_seqlen + kTile * C::NQT - 1) / (kTile * C::NQT));
+  fa_fwd_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, nseq, max_seqlen, s);
+  return launch_fwd_d<128>(tq, tk, tv, p, nseq, max_seqlen, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,88 @@
+// Parameters and launch entry points shared between the C ABI layer and the
+// kernels.  Internal to libfa_gb300.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kTile = 128;           // query rows per Q tile and keys per K/V tile
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// Where a CTA's rows live.  Dense batches: sequence b is rows b*N .. b*N+N-1
+// of the [B*N, H, d] view and TMA coordinates use (row, b) with the batch as
+// the outer tensor dimension, so reads past N zero-fill.  Packed batches:
+// sequence s is rows cu[s] .. cu[s+1]-1 of the single [total, H, d] tensor.
+struct SeqView {
+  const int* cu_seqlens;  // device [nseq + 1] or nullptr for a dense batch
+  int H;
+  int N;                  // dense: rows per sequence; packed: total rows
+  int lse_stride;         // N (dense) or max_seqlen (packed)
+};
+
+struct FwdParams {
+  SeqView sv;
+  uint16_t* o;            // bf16 [.., H, d]
+  float* lse;             // fp32 [nseq|B, H, lse_stride]
+  float scale_log2;       // scale * log2(e)
+  int causal;
+  uint32_t* err;          // device error word
+  uint64_t timeout_ns;
+};
+
+struct BwdParams {
+  SeqView sv;
+  const uint16_t* o;
+  const uint16_t* dout;
+  const float* lse;
+  float* dpsum;           // D = rowsum(dO * O), fp32 [nseq|B, H, lse_stride]
+  float* dq_accum;        // fp32, same layout as q
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  float scale;
+  float scale_log2;
+  int causal;
+  int rows;               // B*N (dense) or total (packed): rows of the [rows, H, d] view
+  int nseq;               // B (dense) or nseq (packed)
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+// Position of a CTA's (sequence, head): blockIdx.x = sequence * H + head.
+struct SeqPos {
+  int bs, h, seq_start, seqlen, row_base, tma_row0, tma_b;
+};
+
+__device__ __forceinline__ SeqPos seq_pos(const SeqView& sv) {
+  SeqPos s;
+  s.bs = blockIdx.x / sv.H;
+  s.h = blockIdx.x % sv.H;
+  if (sv.cu_seqlens) {
+    s.seq_start = __ldg(sv.cu_seqlens + s.bs);
+    s.seqlen = __ldg(sv.cu_seqlens + s.bs + 1) - s.seq_start;
+    s.row_base = s.seq_start;
+    s.tma_row0 = s.seq_start;
+    s.tma_b = 0;
+  } else {
+    s.seq_start = 0;
+    s.seqlen = sv.N;
+    s.row_base = s.bs * sv.N;
+    s.tma_row0 = 0;
+    s.tma_b = s.bs;
+  }
+  return s;
+}
+
+// Grid sizes / launches (defined next to the kernels).
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s);
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int max_seqlen, cudaStream_t s,
+                       cudaEvent_t main_start = nullptr, cudaEvent_t main_end = nullptr);
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace fa

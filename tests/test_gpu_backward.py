@@ -1,0 +1,112 @@
+"""Backward parity: CUDA path vs the fp64 oracle on the same seeded bf16
+inputs.  The CUDA backward consumes the CUDA forward's O and LSE (as a caller
+would); the oracle recomputes everything from Q, K, V, dO."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_attention_flash_gb300 import workloads as wl
+from tests.gpu_util import GRAD_RTOL, assert_no_device_error, f64, gpu, rel_fro, require_gpu
+
+pytestmark = gpu
+
+SHAPES = [
+    (1, 1, 1, 64), (1, 2, 127, 64), (2, 3, 129, 128), (1, 2, 256, 128), (2, 2, 300, 64), (1, 3, 513, 128),
+    (1, 2, 1000, 64),
+]
+
+
+def _run(fa, q, k, v, do, causal, scale=None):
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention_forward(qc, kc, vc, causal, scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, doc, lse, causal, scale)
+    torch.cuda.synchronize()
+    assert_no_device_error(fa)
+    return f64(dq), f64(dk), f64(dv)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d", SHAPES)
+def test_backward_matches_oracle(B, H, N, d, causal):
+    fa = require_gpu()
+    q, k, v, do = wl.make_inputs(B, N, H, d, seed=2 * N + d)
+    dq, dk, dv = _run(fa, q, k, v, do, causal)
+    DQ, DK, DV = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, causal)
+    for name, got, ref in (("dq", dq, DQ), ("dk", dk, DK), ("dv", dv, DV)):
+        assert rel_fro(got, ref) <= GRAD_RTOL, (name, rel_fro(got, ref))
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "small_noncausal"])
+def test_backward_small_workloads_full(name):
+    fa = require_gpu()
+    w = wl.WORKLOADS[name]
+    q, k, v, do = wl.workload_inputs(w, seed=0)
+    dq, dk, dv = _run(fa, q, k, v, do, w.causal)
+    DQ, DK, DV = oracle.backward(f64(q), f64(k), f64(v), f64(do), w.scale, w.causal)
+    for nm, got, ref in (("dq", dq, DQ), ("dk", dk, DK), ("dv", dv, DV)):
+        assert rel_fro(got, ref) <= GRAD_RTOL, (nm, rel_fro(got, ref))
+
+
+@pytest.mark.parametrize("name", ["mid_n4096_d128", "long_n32768"])
+def test_backward_full_size_sampled(name):
+    """Full-size workload in the benchmark's launch configuration.  Sampled
+    dQ rows anywhere; dK/dV rows from the tail of the sequence (causal: few
+    query rows see them) and a few from the start for one head; invariants
+    that hold at any size on every head."""
+    fa = require_gpu()
+    w = wl.WORKLOADS[name]
+    q, k, v, do = wl.workload_inputs(w, seed=0)
+    dq, dk, dv = _run(fa, q, k, v, do, w.causal)
+    qd, kd, vd, dod = f64(q), f64(k), f64(v), f64(do)
+    rng = np.random.default_rng(7)
+    for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+        rows = np.unique(np.concatenate([[0, 127, 128, w.N - 1], rng.integers(0, w.N, 24)]))
+        keys = np.unique(np.concatenate([[w.N - 1, w.N - 128, w.N - 129], rng.integers(w.N - 256, w.N, 12)]))
+        DQ, DK, DV = oracle.backward_rows(qd, kd, vd, dod, w.scale, w.causal, b, h, rows, keys)
+        assert rel_fro(dq[b, rows, h], DQ) <= GRAD_RTOL
+        assert rel_fro(dk[b, keys, h], DK) <= GRAD_RTOL
+        assert rel_fro(dv[b, keys, h], DV) <= GRAD_RTOL
+    if w.N <= 4096:
+        keys = np.array([0, 1, 127, 128, 1000])
+        _, DK, DV = oracle.backward_rows(qd, kd, vd, dod, w.scale, w.causal, 0, 1, [], keys)
+        assert rel_fro(dk[0, keys, 1], DK) <= GRAD_RTOL
+        assert rel_fro(dv[0, keys, 1], DV) <= GRAD_RTOL
+    # Rows of P sum to one: sum_j dV_j = sum_i dO_i.  Rows of dS sum to zero:
+    # sum_j dK_j = 0.  Both per (batch, head), at full size.
+    sdv, sdo = dv.sum(axis=1), dod.sum(axis=1)
+    assert np.abs(sdv - sdo).max() <= 2e-2 * np.abs(sdo).max() + 1e-2 * np.sqrt(w.N)
+    sdk = dk.sum(axis=1)
+    assert np.abs(sdk).max() <= 2e-2 * np.abs(dk).max() * np.sqrt(w.N)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+def test_backward_repeatable_and_workspace_reuse():
+    """dQ is accumulated with atomics: results vary only by rounding order;
+    a dirty reused workspace must not leak into the result."""
+    fa = require_gpu()
+    B, N, H, d = 1, 640, 2, 128
+    q, k, v, do = wl.make_inputs(B, N, H, d, seed=99)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention_forward(qc, kc, vc, True)
+    ws = torch.full((fa.fa_bwd_workspace_bytes(B, H, N, d),), 0x7F, device="cuda", dtype=torch.uint8)
+    r1 = fa.attention_backward(qc, kc, vc, o, doc, lse, True, workspace=ws)
+    r2 = fa.attention_backward(qc, kc, vc, o, doc, lse, True, workspace=ws)
+    for a, b in zip(r1, r2):
+        assert rel_fro(f64(a), f64(b)) <= 1e-2
+    DQ, DK, DV = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, True)
+    for got, ref in zip(r2, (DQ, DK, DV)):
+        assert rel_fro(f64(got), ref) <= GRAD_RTOL
+
+
+def test_autograd_function():
+    fa = require_gpu()
+    B, N, H, d = 1, 300, 2, 64
+    q, k, v, do = wl.make_inputs(B, N, H, d, seed=4)
+    tq, tk, tv = (t.cuda().requires_grad_() for t in (q, k, v))
+    out = fa.flash_attention(tq, tk, tv, causal=True)
+    out.backward(do.cuda())
+    DQ, DK, DV = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, True)
+    assert rel_fro(f64(tq.grad), DQ) <= GRAD_RTOL
+    assert rel_fro(f64(tk.grad), DK) <= GRAD_RTOL
+    assert rel_fro(f64(tv.grad), DV) <= GRAD_RTOL
