@@ -344,13 +344,30 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
     return {"ms": statistics.mean(times), "h2d": h2d, "d2h": d2h}
 
 
+KERNEL_SOURCES = {
+    "fa_bwd_main_kernel": ["fa_bwd.cu", "ptx.cuh", "fa_kernels.cuh"],
+    "fa_fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "fa_kernels.cuh"],
+}
+
+
 def _committed_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one
-    exists for this workload (profiles/<kernel>__<workload>.json)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/<kernel>__<workload>.json), or None when there is none or the
+    kernel's sources changed since the counters were taken (the summary
+    records a SHA-256 of those sources)."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.json")
     try:
         with open(path) as f:
-            return json.load(f).get("dram_bytes_per_launch")
+            summary = json.load(f)
+        h = hashlib.sha256()
+        for name in KERNEL_SOURCES[kernel]:
+            with open(os.path.join(ROOT, "io_aware_attention_flash_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if summary.get("source_sha256") != h.hexdigest():
+            return None
+        return summary.get("dram_bytes_per_launch")
     except Exception:
         return None
 

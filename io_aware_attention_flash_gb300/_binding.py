@@ -169,6 +169,12 @@ def fa_get_device_error(stream=None) -> int:
 def fa_set_kernel_events(start_event, end_event) -> None:
     """Time the main kernel of the next backward call on this thread with two
     torch.cuda.Event objects (created with enable_timing=True)."""
+    for ev in (start_event, end_event):
+        # torch creates the underlying cudaEvent_t lazily, on the first
+        # record; record once so there is a handle (and torch regards the
+        # event as recorded).  The library records it again around the kernel.
+        if ev is not None and ev.cuda_event == 0:
+            ev.record()
     s = None if start_event is None else ctypes.c_void_p(start_event.cuda_event)
     e = None if end_event is None else ctypes.c_void_p(end_event.cuda_event)
     _check("fa_set_kernel_events", lib().fa_set_kernel_events(s, e))
