@@ -69,7 +69,8 @@ enum {
   FA_ERR_TIMEOUT = 7,       /* a kernel's bounded wait expired (device side) */
   FA_ERR_WORKSPACE = 8,     /* workspace missing or smaller than required */
   FA_ERR_SCALE = 9,         /* scale not finite */
-  FA_ERR_NOT_DEVICE = 10    /* q is not device memory (its device is the one launched on) */
+  FA_ERR_NOT_DEVICE = 10,   /* q is not device memory (its device is the one launched on) */
+  FA_ERR_SCRATCH_LIMIT = 11 /* fa_bwd_noalloc: problem needs more than FA_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -165,6 +166,41 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  * Passing NULL for both clears a pending hook.
  */
 FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event);
+
+/*
+ * Backward, dense batch, without a caller-supplied workspace.  (The pages
+ * have no counterpart: this is a deployment convenience.)
+ *
+ * Some callers cannot allocate device memory at the point where they need
+ * the backward: a plugin running inside a host framework that owns all
+ * device memory and hands the plugin no workspace, or a latency-critical
+ * path where allocating is forbidden because it can synchronise the device
+ * or fail under fragmentation.  This entry point serves them: it takes the
+ * same arguments as fa_bwd minus the workspace and allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).  Its scratch — the D
+ * row statistic and the fp32 dQ accumulator, exactly what
+ * fa_bwd_workspace_bytes() sizes — lives in one file-scope static device
+ * array of FA_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the
+ * library holds until the process exits.
+ *
+ *   - Limit: problems whose fa_bwd_workspace_bytes(B, H, N, d) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_SCRATCH_LIMIT before
+ *     anything is enqueued (e.g. B=1, H=8, N=4096, d=128 needs 16.9 MB and
+ *     fits; B=1, H=16, N=4096, d=128 needs 33.8 MB and does not).
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array.  The kernels
+ *     re-initialise the parts that must start at zero on every call, so stale
+ *     contents from an earlier call do not leak in, but two calls that
+ *     overlap on the GPU (different streams, or concurrent host threads)
+ *     race on the array and produce wrong gradients: serialise them.
+ * Other arguments, layouts and errors are those of fa_bwd.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                float scale, int causal, void* stream);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_HEAD_DIM", 4: "FA_ERR_SHAPE",
     5: "FA_ERR_ARCH", 6: "FA_ERR_CUDA", 7: "FA_ERR_TIMEOUT", 8: "FA_ERR_WORKSPACE", 9: "FA_ERR_SCALE",
-    10: "FA_ERR_NOT_DEVICE",
+    10: "FA_ERR_NOT_DEVICE", 11: "FA_ERR_SCRATCH_LIMIT",
 }
 
 # Exported symbols and their C signatures (include/fa.h).
@@ -38,7 +38,11 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_I, [_U64, _P]),
     "fa_set_kernel_events": (_I, [_P, _P]),
     "fa_last_error_detail": (ctypes.c_char_p, []),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
 }
+
+# Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -130,6 +134,19 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale=Non
     _check("fa_bwd", lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
                                   _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   B, H, N, d, _scale(scale, d), int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale=None, stream=None) -> None:
+    """fa_bwd for callers that cannot provide device memory: the library's
+    static scratch array stands in for the workspace (problems up to
+    NOALLOC_SCRATCH_BYTES of workspace; calls must not overlap on the GPU)."""
+    B, N, H, d = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _bf16(n, t, (B, N, H, d))
+    _f32("lse", lse, (B, H, N))
+    _check("fa_bwd_noalloc", lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                                  _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, _scale(scale, d),
+                                                  int(bool(causal)), _stream(stream)))
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale=None, stream=None) -> None:

@@ -270,6 +270,7 @@ FA_API const char* fa_status_string(fa_status status) {
     case FA_ERR_WORKSPACE: return "workspace missing or too small";
     case FA_ERR_SCALE: return "scale is not finite";
     case FA_ERR_NOT_DEVICE: return "q is not a device pointer";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the static no-alloc array holds";
     default: return "unknown status";
   }
 }
@@ -338,6 +339,56 @@ FA_API fa_status fa_get_device_error(void* stream) {
 }
 
 FA_API const char* fa_last_error_detail(void) { return t_detail; }
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of fa_bwd_noalloc: D and the fp32 dQ accumulator for callers that
+// cannot hand the library a workspace.  File-scope static device storage:
+// every GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  In host code the array's name is only a host-side stand-in,
+// so kernels must be given this address, never the name.
+fa_status noalloc_scratch(void** out) {
+  static void* cache[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail("device ordinal out of range", cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail("cudaGetSymbolAddress(no-alloc scratch)", e);
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                float scale, int causal, void* stream) {
+  FA_TRY(check_common(H, d, scale));
+  if (B <= 0 || N <= 0) return FA_ERR_SHAPE;
+  FA_TRY(check_rows(B, static_cast<long long>(B) * N, N, H, d));
+  const size_t need = bwd_ws_bytes(static_cast<long long>(B) * H * N, static_cast<long long>(B) * N, H, d);
+  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  if (!q) return FA_ERR_NULL;
+  FA_TRY(bind_device(q));  // the scratch address is per device: look it up with q's device current
+  void* scratch = nullptr;
+  FA_TRY(noalloc_scratch(&scratch));
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, scratch, FA_NOALLOC_SCRATCH_BYTES, nullptr, B, N, N, B, H, d,
+                  scale, causal, stream);
+}
 
 FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event) {
   if ((start_event == nullptr) != (end_event == nullptr)) return FA_ERR_NULL;

@@ -104,3 +104,12 @@ def test_valid_arguments_without_gpu_report_cuda_or_arch(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; the GPU tests cover valid calls")
     assert _fwd(lib) in (5, 6, 10)
+
+
+def test_noalloc_limit_matches_header_and_rejects_on_host(lib):
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == _binding.NOALLOC_SCRATCH_BYTES
+    # 33.8 MB of workspace needed: rejected before any CUDA call
+    assert lib.fa_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              1, 16, 4096, 128, 0.1, 1, None) == 11
