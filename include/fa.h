@@ -157,6 +157,22 @@ FA_API const char* fa_last_error_detail(void);
 FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
 /*
+ * Unit-rate microbenchmarks for the MUFU-vs-tensor argument ("LLM Systems
+ * 22: Flash Attention", section 4.1.2: exponential cycles against GEMM
+ * cycles; section 4.2: how the two rates scale on Blackwell).  Runs one CTA
+ * per SM on the current device, synchronises `stream`, and writes to
+ * *result the rate per SM per SM-clock (measured with the SM cycle counter):
+ *   which = 0: ex2.approx.f32 results per SM-clock
+ *           1: cvt.rn.bf16x2.f32 conversions per SM-clock
+ *           2: fp32 FMAs per SM-clock
+ *           3: tcgen05.mma bf16 FLOPs per SM-clock, M=128 N=256 K=16, SMEM operands
+ *           4: the same with N=128
+ * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
+ * unknown `which` or out-of-range `iters`.
+ */
+FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream);
+
+/*
  * Kernel timing hook (no counterpart on the pages; for measurement only).
  * Makes the next fa_bwd / fa_bwd_varlen call issued from this host thread
  * record `start_event` immediately before and `end_event` immediately after

@@ -39,7 +39,12 @@ SIGNATURES = {
     "fa_set_kernel_events": (_I, [_P, _P]),
     "fa_last_error_detail": (ctypes.c_char_p, []),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_microbench": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double), _P]),
 }
+
+# fa_microbench selectors: rate per SM per SM-clock of each unit.
+MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk": 2,
+              "mma_bf16_flop_per_sm_clk_n256": 3, "mma_bf16_flop_per_sm_clk_n128": 4}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -199,3 +204,10 @@ def fa_set_kernel_events(start_event, end_event) -> None:
 
 def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib().fa_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def fa_microbench(name: str, iters: int, stream=None) -> float:
+    """Rate per SM per clock of one unit (see MICROBENCH for the names)."""
+    out = ctypes.c_double(0.0)
+    _check("fa_microbench", lib().fa_microbench(MICROBENCH[name], int(iters), ctypes.byref(out), _stream(stream)))
+    return out.value

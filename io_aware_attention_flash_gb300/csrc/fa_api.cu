@@ -407,4 +407,14 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   return e == cudaSuccess ? FA_OK : cuda_fail("self-test launch", e);
 }
 
+FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
+  if (!result) return FA_ERR_NULL;
+  if (which < 0 || which > 4 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  FA_TRY(check_arch());
+  uint32_t* err = nullptr;
+  FA_TRY(error_word(&err));
+  const cudaError_t e = fa::run_microbench(which, iters, err, result, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("microbenchmark", e);
+}
+
 }  // extern "C"

@@ -1,0 +1,153 @@
+// Unit-rate microbenchmarks behind the MUFU-vs-tensor argument of "LLM
+// Systems 22: Flash Attention", sections 4.1.2 and 4.2: per SM and per clock,
+// how many exponentials the special-function unit retires (ex2.approx) and how
+// many bf16 FLOPs tcgen05.mma retires.  Each kernel times itself with the SM
+// cycle counter, so the results are in units per SM-clock whatever the clock.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_kernels.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kChains = 8;  // independent dependency chains per thread
+constexpr int kMaxSms = 1024;
+
+// Per-CTA cycle counts (one CTA per SM) and a sink that keeps the timed loops
+// from being optimised away.
+__device__ unsigned long long g_cycles[kMaxSms];
+__device__ float g_sink[kMaxSms];
+
+// kind 0: ex2.approx.ftz.f32; 1: cvt.rn.bf16x2.f32; 2: fma.rn.f32.
+template <int KIND>
+__global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned long long* cycles, float* sink) {
+  float x[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) x[c] = -1.0f - 0.001f * (threadIdx.x + c);
+  __syncthreads();
+  const unsigned long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) {
+      if constexpr (KIND == 0) {
+        x[c] = ex2_approx(x[c]) - 1.5f;  // stays in (-1.5, -0.5): no denormals or overflow
+      } else if constexpr (KIND == 1) {
+        const uint32_t p = pack_bf16x2(x[c], x[c] + 1.0f);
+        x[c] = __uint_as_float(p & 0xFFFF0000u) * 0.5f - 0.75f;
+      } else {
+        x[c] = fmaf(x[c], 0.999f, -0.001f);
+      }
+    }
+  }
+  __syncthreads();
+  const unsigned long long t1 = clock64();
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) s += x[c];
+  if (s == 12345.f) sink[threadIdx.x % kMaxSms] = s;  // keeps the loop alive
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+// tcgen05.mma throughput: one thread issues `iters` x 4 MMAs of M=128, N, K=16
+// (bf16, both operands in shared memory, fp32 accumulate in TMEM) and waits
+// for them to finish.  Operand contents are zero: only the rate matters.
+template <int N>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t tmem_slot;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gen = smem_raw + (base - raw);
+  const int warp = threadIdx.x / 32;
+  for (int i = threadIdx.x; i < (128 + N) * 128 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gen)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done_bar), 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = idesc_bf16(128, N, false, false);
+    const uint32_t sA = base, sB = base + 128 * 128;
+    const unsigned long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tmem, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 32, 16, 1024), idesc,
+               (i | kk) ? 1u : 0u);
+    }
+    tc_commit(smem_u32(&done_bar));
+    wait_drain(smem_u32(&done_bar), 0, err, 2000000000ull);
+    const unsigned long long t1 = clock64();
+    cycles[blockIdx.x] = t1 - t0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+template <int N>
+cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
+  const int smem = (128 + N) * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mma_rate_kernel<N><<<sms, 128, smem, s>>>(iters, cyc, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Runs one microbenchmark with one CTA per SM and returns the mean over CTAs
+// of (units retired by the CTA) / (its SM cycles).
+cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (sms > kMaxSms) sms = kMaxSms;
+  unsigned long long* cyc = nullptr;
+  float* sink = nullptr;
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&cyc), g_cycles)) != cudaSuccess) return e;
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&sink), g_sink)) != cudaSuccess) return e;
+  double units_per_cta = 0;
+  const int threads = 1024;
+  switch (which) {
+    case 0: unit_rate_kernel<0><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 1: unit_rate_kernel<1><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 2: unit_rate_kernel<2><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 3: e = launch_mma_rate<256>(sms, iters, cyc, err, s); break;
+    case 4: e = launch_mma_rate<128>(sms, iters, cyc, err, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  if (which <= 2)
+    units_per_cta = static_cast<double>(threads) * iters * kChains;
+  else
+    units_per_cta = 2.0 * 128 * (which == 3 ? 256 : 128) * 64 * static_cast<double>(iters);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  static unsigned long long host_cyc[kMaxSms];
+  if ((e = cudaMemcpy(host_cyc, cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return e;
+  double acc = 0;
+  for (int i = 0; i < sms; ++i) acc += units_per_cta / static_cast<double>(host_cyc[i] ? host_cyc[i] : 1);
+  *result = acc / sms;
+  return cudaSuccess;
+}
+
+}  // namespace fa
