@@ -89,8 +89,9 @@ FA_API const char* fa_status_string(fa_status status);
 FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, void* stream);
 
-/* Bytes of fp32 workspace fa_bwd needs: D [B, H, N] and the dQ accumulator
- * [B, N, H, d], each padded to 256 bytes. */
+/* Bytes of fp32 workspace fa_bwd needs: D [B, H, N] (padded to 256 bytes)
+ * followed by the dQ accumulator, H·d values for each of B·N rows rounded up
+ * to a multiple of 128 (an internal tiled layout). */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
@@ -122,8 +123,9 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
 FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                         int nseq, int max_seqlen, int total, int H, int d, float scale, int causal, void* stream);
 
-/* Workspace for fa_bwd_varlen: D [nseq, H, max_seqlen] and the dQ
- * accumulator [total, H, d], fp32, each padded to 256 bytes. */
+/* Workspace for fa_bwd_varlen: D [nseq, H, max_seqlen] (padded to 256 bytes)
+ * and the fp32 dQ accumulator for `total` rows rounded up to a multiple of
+ * 128, H·d values each. */
 FA_API size_t fa_bwd_varlen_workspace_bytes(int total, int nseq, int max_seqlen, int H, int d);
 
 /* Backward, packed variable-length batch; arguments as fa_bwd and

@@ -182,8 +182,11 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
 }
 
+// D (fp32, stat_elems) then the fp32 dQ accumulator, tiled by 128 rows (rows
+// rounded up to a multiple of 128).
 size_t bwd_ws_bytes(long long stat_elems, long long rows, int H, int d) {
-  return pad256(static_cast<size_t>(stat_elems) * 4) + pad256(static_cast<size_t>(rows) * H * d * 4);
+  const size_t rows128 = static_cast<size_t>((rows + fa::kTile - 1) / fa::kTile) * fa::kTile;
+  return pad256(static_cast<size_t>(stat_elems) * 4) + rows128 * H * d * 4;
 }
 
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

@@ -21,9 +21,10 @@
 //                the fp32 accumulator with vector atomics (other key tiles add
 //                to the same rows).
 //   fa_bwd_post  dQ = bf16(scale · dQ_accum).
-// Warp roles in fa_bwd_main: warps 0-3 recompute P and dS (thread r owns key
-// row r = TMEM lane r), warps 4-7 drain dQ and write dV, warp 8 issues TMA,
-// warp 9 issues tcgen05.mma.
+// Warp roles in fa_bwd_main: warps 0-7 (two warpgroups, each owning half of
+// the query columns of a tile; thread r owns key row r = TMEM lane r)
+// recompute P and dS, drain dQ and write dK / dV; warp 8 issues TMA; warp 9
+// issues tcgen05.mma.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,6 +58,20 @@ __device__ __forceinline__ void locate_row(const SeqView& sv, int nseq, int g, i
 }
 
 // ----------------------------------------------------------------------------
+// The fp32 dQ accumulator is tiled by 128 global rows: element (row R, head h,
+// column k) lives at
+//   ((⌊R/128⌋·H + h)·(d/4) + ⌊k/4⌋)·512 + (R mod 128)·4 + (k mod 4)
+// so the 16-byte chunk k/4 of 128 consecutive rows is contiguous.  A warp of
+// the dQ drain (lanes = 32 consecutive query rows, each adding the same column
+// chunk) then touches 512 contiguous bytes per vector atomic instead of 32
+// rows 8 KB apart.
+// ----------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ size_t dq_index(int R, int h, int H, int chunk4) {
+  return ((static_cast<size_t>(R >> 7) * H + h) * (D / 4) + chunk4) * 512 + static_cast<size_t>(R & 127) * 4;
+}
+
+// ----------------------------------------------------------------------------
 // fa_bwd_pre: one warp per (row, head).
 // ----------------------------------------------------------------------------
 template <int D>
@@ -74,12 +89,13 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
     const uint2 d = *reinterpret_cast<const uint2*>(p.dout + base + lane * 4);
     acc = bf16lo_to_f32(o.x) * bf16lo_to_f32(d.x) + bf16hi_to_f32(o.x) * bf16hi_to_f32(d.x) +
           bf16lo_to_f32(o.y) * bf16lo_to_f32(d.y) + bf16hi_to_f32(o.y) * bf16hi_to_f32(d.y);
-    *reinterpret_cast<float4*>(p.dq_accum + base + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(p.dq_accum + dq_index<D>(g, h, H, lane)) = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
     const uint32_t o = *reinterpret_cast<const uint32_t*>(p.o + base + lane * 2);
     const uint32_t d = *reinterpret_cast<const uint32_t*>(p.dout + base + lane * 2);
     acc = bf16lo_to_f32(o) * bf16lo_to_f32(d) + bf16hi_to_f32(o) * bf16hi_to_f32(d);
-    *reinterpret_cast<float2*>(p.dq_accum + base + lane * 2) = make_float2(0.f, 0.f);
+    *reinterpret_cast<float2*>(p.dq_accum + dq_index<D>(g, h, H, lane >> 1) + (lane & 1) * 2) =
+        make_float2(0.f, 0.f);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -91,25 +107,39 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
 }
 
 // ----------------------------------------------------------------------------
-// fa_bwd_post: 8 elements per thread.
+// fa_bwd_post: dQ = bf16(scale · accumulator).  Grid (row tiles, H, d/8),
+// 128 threads: thread = row of the tile, 8 columns each (two 16-byte chunks of
+// the tiled accumulator, read coalesced across the block).
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const BwdParams p, size_t n8) {
-  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(p.dq_accum)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(p.dq_accum)[2 * i + 1];
+template <int D>
+__global__ void __launch_bounds__(128) fa_bwd_post_kernel(const BwdParams p) {
+  const int R = blockIdx.x * 128 + threadIdx.x;
+  if (R >= p.rows) return;
+  const int h = blockIdx.y, c8 = blockIdx.z;
+  const int H = p.sv.H;
+  const float4 a = *reinterpret_cast<const float4*>(p.dq_accum + dq_index<D>(R, h, H, 2 * c8));
+  const float4 b = *reinterpret_cast<const float4*>(p.dq_accum + dq_index<D>(R, h, H, 2 * c8 + 1));
   const float s = p.scale;
   uint4 w;
   w.x = pack_bf16x2(a.x * s, a.y * s);
   w.y = pack_bf16x2(a.z * s, a.w * s);
   w.z = pack_bf16x2(b.x * s, b.y * s);
   w.w = pack_bf16x2(b.z * s, b.w * s);
-  reinterpret_cast<uint4*>(p.dq)[i] = w;
+  *reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(R) * H + h) * D + 8 * c8) = w;
 }
 
 // ----------------------------------------------------------------------------
 // fa_bwd_main
 // ----------------------------------------------------------------------------
+// TMEM holds dV and dK (d columns each) for the whole loop plus two 128-column
+// regions R0, R1 that alternate roles from one query tile to the next:
+//   tile i: Sᵀ_i -> R[i&1] (then Pᵀ_i as bf16, then dQ_i)
+//           dPᵀ_i -> R[(i+1)&1] (then dSᵀ_i as bf16)
+// so Sᵀ_{i+1} can be computed into R[(i+1)&1] as soon as dK_i has read dSᵀ_i,
+// while the compute warps drain dQ_i out of R[i&1]; dPᵀ_{i+1} then reuses
+// R[i&1].  MMA order per tile: dV_i, dK_i, dQ_i, Sᵀ_{i+1}, dPᵀ_{i+1}.  The
+// compute warps overlap Pᵀ_{i+1} with dPᵀ_{i+1}, dSᵀ_{i+1} with dV_{i+1}, and
+// the dQ_i drain with Sᵀ_{i+1}.
 template <int D>
 struct BwdCfg {
   static constexpr int KB = D / 64;
@@ -129,24 +159,26 @@ struct BwdCfg {
   static constexpr int B_QEMPTY = B_DOFULL + NSQ;
   static constexpr int B_SFULL = B_QEMPTY + NSQ;
   static constexpr int B_DPFULL = B_SFULL + 1;
-  static constexpr int B_DSREADY = B_DPFULL + 1;
+  static constexpr int B_PREADY = B_DPFULL + 1;
+  static constexpr int B_DSREADY = B_PREADY + 1;
   static constexpr int B_DQFULL = B_DSREADY + 1;
   static constexpr int B_DQDRAINED = B_DQFULL + 1;
   static constexpr int B_DKDV = B_DQDRAINED + 1;
   static constexpr int B_DRAIN = B_DKDV + 1;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int B_STAT = B_DRAIN + 1;           // [2]: row statistics of a query tile staged
+  static constexpr int NBAR = B_STAT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // Whatever is left of the 227 KB opt-in limit is alignment slack.
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
-  static constexpr int NUM_THREADS = 10 * 32;
+  static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
+  static constexpr int NUM_THREADS = NUM_COMPUTE + 64;
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0;
   static constexpr uint32_t DK_COL = D;
-  static constexpr uint32_t S_COL = 2 * D;             // Sᵀ, then Pᵀ (bf16), then dQ_i
-  static constexpr uint32_t DP_COL = 2 * D + 128;      // dPᵀ, then dSᵀ (bf16)
+  static constexpr uint32_t R_COL = 2 * D;             // R0 = R_COL, R1 = R_COL + 128
   static_assert(SMEM_USED <= 232448, "shared memory budget");
 };
 
@@ -168,7 +200,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);  // [buf][0: lse2, 1: D][128]
+  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);  // [buf][0: log2e·LSE, 1: D][128]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -189,11 +221,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
-    mbar_init(bar(C::B_DSREADY), 128);
+    mbar_init(bar(C::B_PREADY), C::NUM_COMPUTE);
+    mbar_init(bar(C::B_DSREADY), C::NUM_COMPUTE);
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQDRAINED), 128);
+    mbar_init(bar(C::B_DQDRAINED), C::NUM_COMPUTE);
     mbar_init(bar(C::B_DKDV), 1);
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_STAT + 0), C::NUM_COMPUTE);
+    mbar_init(bar(C::B_STAT + 1), C::NUM_COMPUTE);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -255,114 +290,162 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       constexpr uint32_t idesc_sp = idesc_bf16(128, 128, false, false);   // Sᵀ, dPᵀ
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);      // dV, dK (A from TMEM)
       constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);        // dQ (A = dS, MN-major)
-      const uint32_t tS = tmem + C::S_COL, tDP = tmem + C::DP_COL;
-      bool ok = wait_bounded(bar(C::B_KV), 0, abort_flag, p.err, p.timeout_ns);
+      auto region = [&](int r) -> uint32_t { return tmem + C::R_COL + (r & 1) * 128; };
+      auto issue_sp = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
+          mma_ss(dst, sdesc_sw128(a_base + koff, 16, 1024), sdesc_sw128(b_base + koff, 16, 1024), idesc_sp, kk > 0);
+        }
+      };
+      bool ok = wait_bounded(bar(C::B_KV), 0, abort_flag, p.err, p.timeout_ns) &&
+                wait_bounded(bar(C::B_QFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_sp(region(0), sb + C::OFF_K, sb + C::OFF_Q);                 // Sᵀ_0 -> R0
+        tc_commit(bar(C::B_SFULL));
+        ok = wait_bounded(bar(C::B_DOFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_sp(region(1), sb + C::OFF_V, sb + C::OFF_DO);                // dPᵀ_0 -> R1
+        tc_commit(bar(C::B_DPFULL));
+      }
       for (int ii = 0; ok && ii < nq; ++ii) {
         const int qs = ii % C::NSQ;
-        const uint32_t ph = (ii / C::NSQ) & 1;
         const uint32_t sQ = sb + C::OFF_Q + qs * C::TILE_BYTES;
         const uint32_t sdO = sb + C::OFF_DO + qs * C::TILE_BYTES;
-        ok = wait_bounded(bar(C::B_QFULL + qs), ph, abort_flag, p.err, p.timeout_ns);
-        if (ok && ii > 0) ok = wait_bounded(bar(C::B_DQDRAINED), (ii - 1) & 1, abort_flag, p.err, p.timeout_ns);
+        const uint32_t rs = region(ii), rp = region(ii + 1);
+        ok = wait_bounded(bar(C::B_PREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
-          mma_ss(tS, sdesc_sw128(sb + C::OFF_K + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024), idesc_sp,
-                 kk > 0);
-        }
-        tc_commit(bar(C::B_SFULL));
-        if (!wait_bounded(bar(C::B_DOFULL + qs), ph, abort_flag, p.err, p.timeout_ns)) break;
+        for (int kk = 0; kk < kTile / 16; ++kk)  // dV += Pᵀ dO_i (Pᵀ packed in rs)
+          mma_ts(tmem + C::DV_COL, rs + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(sdO + kk * 2048, C::BLK_BYTES, 1024), idesc_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+        ok = wait_bounded(bar(C::B_DSREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
-          mma_ss(tDP, sdesc_sw128(sb + C::OFF_V + koff, 16, 1024), sdesc_sw128(sdO + koff, 16, 1024), idesc_sp,
-                 kk > 0);
-        }
-        tc_commit(bar(C::B_DPFULL));
-        if (!wait_bounded(bar(C::B_DSREADY), ii & 1, abort_flag, p.err, p.timeout_ns)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t moff = kk * 2048;  // 16 query rows of the MN-major operand
-          mma_ts(tmem + C::DV_COL, tS + kk * 8, sdesc_sw128(sdO + moff, C::BLK_BYTES, 1024), idesc_kv,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::DK_COL, tDP + kk * 8, sdesc_sw128(sQ + moff, C::BLK_BYTES, 1024), idesc_kv,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dSᵀ Q_i (dSᵀ packed in rp)
+          mma_ts(tmem + C::DK_COL, rp + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(sQ + kk * 2048, C::BLK_BYTES, 1024), idesc_kv, (ii > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(C::B_QEMPTY + qs));
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t moff = kk * 2048;  // 16 key rows
-          mma_ss(tS, sdesc_sw128(sb + C::OFF_DS + moff, C::BLK_BYTES, 1024),
-                 sdesc_sw128(sb + C::OFF_K + moff, C::BLK_BYTES, 1024), idesc_q, kk > 0);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)  // dQ_i = dS K_j -> rs
+          mma_ss(rs, sdesc_sw128(sb + C::OFF_DS + kk * 2048, C::BLK_BYTES, 1024),
+                 sdesc_sw128(sb + C::OFF_K + kk * 2048, C::BLK_BYTES, 1024), idesc_q, kk > 0);
         tc_commit(bar(C::B_DQFULL));
+        if (ii + 1 < nq) {
+          const int qs1 = (ii + 1) % C::NSQ;
+          const uint32_t ph1 = ((ii + 1) / C::NSQ) & 1;
+          ok = wait_bounded(bar(C::B_QFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sp(rp, sb + C::OFF_K, sb + C::OFF_Q + qs1 * C::TILE_BYTES);     // Sᵀ_{i+1} -> rp
+          tc_commit(bar(C::B_SFULL));
+          ok = wait_bounded(bar(C::B_DQDRAINED), ii & 1, abort_flag, p.err, p.timeout_ns);
+          if (!ok) break;
+          ok = wait_bounded(bar(C::B_DOFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sp(rs, sb + C::OFF_V, sb + C::OFF_DO + qs1 * C::TILE_BYTES);    // dPᵀ_{i+1} -> rs
+          tc_commit(bar(C::B_DPFULL));
+        }
       }
       if (ok) tc_commit(bar(C::B_DKDV));
       tc_commit(bar(C::B_DRAIN));
       wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- P, dS
-    const int r = warp * 32 + lane;        // key row within the tile = TMEM lane
+  } else {
+    // ---------------------------------------------------------------- P, dS, dQ drain
+    // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ and dQ columns
+    // g·d/2 .. (g+1)·d/2-1; thread r of a warpgroup owns TMEM lane r.
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;          // key row of Sᵀ / dPᵀ; query row of dQ
     const int kv_row = kv0 + r;
     const bool row_dead = kv_row >= sp.seqlen;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t tS = lane_addr + C::S_COL, tDP = lane_addr + C::DP_COL;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
-    const uint32_t sDS = sb + C::OFF_DS;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int qi = i_first + ii;
       const int q0 = qi * kTile;
+      const uint32_t rs = lane_addr + C::R_COL + (ii & 1) * 128;
+      const uint32_t rp = lane_addr + C::R_COL + ((ii + 1) & 1) * 128;
       float* lse2 = stat + (ii & 1) * 256;
       float* dsum = lse2 + 128;
       {
         const int q = q0 + r;
         const bool valid = q < sp.seqlen;
-        lse2[r] = valid ? __ldg(p.lse + stat_base + q) * kLog2e : CUDART_INF_F;
-        dsum[r] = valid ? __ldg(p.dpsum + stat_base + q) : 0.f;
+        if (g == 0) lse2[r] = valid ? __ldg(p.lse + stat_base + q) * kLog2e : CUDART_INF_F;
+        else dsum[r] = valid ? __ldg(p.dpsum + stat_base + q) : 0.f;
       }
-      named_bar_sync(1, 128);
-      ok = wait_bounded(bar(C::B_SFULL), ii & 1, abort_flag, p.err, p.timeout_ns) &&
-           wait_bounded(bar(C::B_DPFULL), ii & 1, abort_flag, p.err, p.timeout_ns);
-      if (ok && ii > 0) ok = wait_bounded(bar(C::B_DQFULL), (ii - 1) & 1, abort_flag, p.err, p.timeout_ns);
-      if (!ok) break;
-      tc_fence_after();
+      // Both warpgroups read all 128 entries: publish them through an mbarrier
+      // (a bounded wait, unlike a named barrier, so an abort cannot hang here).
+      mbar_arrive(bar(C::B_STAT + (ii & 1)));
+      if (!wait_bounded(bar(C::B_STAT + (ii & 1)), (ii >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
       const bool need_mask = row_dead || (p.causal && qi == j);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tS + ch * 32, s);
-        tmem_ld32(tDP + ch * 32, dp);
+      // ---- Pᵀ = 2^(c·Sᵀ − log2e·LSE) for this warpgroup's 64 query columns
+      if (!wait_bounded(bar(C::B_SFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pr[2][32];
+      tmem_ld32(rs + 64 * g, pr[0]);
+      tmem_ld32(rs + 64 * g + 32, pr[1]);
+      tmem_wait_ld();
+      reg_fence(pr[0]);
+      reg_fence(pr[1]);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = 64 * g + 32 * ch + e;
+          float pe = ex2_approx(fmaf(__uint_as_float(pr[ch][e]), c, -lse2[col]));
+          if (need_mask && (row_dead || q0 + col < kv_row)) pe = 0.f;
+          pr[ch][e] = __float_as_uint(pe);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(pr[ch][2 * e]), __uint_as_float(pr[ch][2 * e + 1]));
+        tmem_st16(rs + 64 * g + 16 * ch, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PREADY));
+      // ---- dSᵀ = Pᵀ ∘ (dPᵀ − D)
+      if (!wait_bounded(bar(C::B_DPFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dp[32];
+        tmem_ld32(rp + 64 * g + 32 * ch, dp);
         tmem_wait_ld();
-        reg_fence(s);
         reg_fence(dp);
-        uint32_t pk[16], dk[16];
+        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = ch * 32 + 2 * e + u;
-            float pe = ex2_approx(fmaf(__uint_as_float(s[2 * e + u]), c, -lse2[col]));
-            if (need_mask && (row_dead || q0 + col < kv_row)) pe = 0.f;
-            pv[u] = pe;
-            dv[u] = pe * (__uint_as_float(dp[2 * e + u]) - dsum[col]);
-          }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk[e] = pack_bf16x2(dv[0], dv[1]);
+          const int col = 64 * g + 32 * ch + 2 * e;
+          const float d0 = __uint_as_float(pr[ch][2 * e]) * (__uint_as_float(dp[2 * e]) - dsum[col]);
+          const float d1 = __uint_as_float(pr[ch][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - dsum[col + 1]);
+          dk[e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(tS + ch * 16, pk);
-        tmem_st16(tDP + ch * 16, dk);
-        // dSᵀ row r, query columns ch*32 .. ch*32+31 -> 128-byte swizzled block (ch / 2)
-        const uint32_t rowaddr = sDS + (ch >> 1) * C::BLK_BYTES + r * 128;
+        tmem_st16(rp + 64 * g + 16 * ch, dk);
+        // dSᵀ row r, query columns 64g+32ch .. +31 -> swizzled SMEM block g (the dQ GEMM's A operand)
+        const uint32_t rowaddr = sb + C::OFF_DS + g * C::BLK_BYTES + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t chunk = ((ch & 1) * 4 + u) ^ (r & 7);
+          const uint32_t chunk = (ch * 4 + u) ^ (r & 7);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + chunk * 16), "r"(dk[4 * u]),
                        "r"(dk[4 * u + 1]), "r"(dk[4 * u + 2]), "r"(dk[4 * u + 3])
                        : "memory");
@@ -372,82 +455,54 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-    }
-    if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
-    if (ok) {
-      tc_fence_after();
-      uint16_t* dst = p.dk + (static_cast<size_t>(sp.row_base) + kv_row) * row_stride + static_cast<size_t>(sp.h) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t a[32];
-        tmem_ld32(lane_addr + C::DK_COL + ch * 32, a);
-        tmem_wait_ld();
-        reg_fence(a);
-        if (!row_dead) {
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
-            w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
-            w.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * p.scale, __uint_as_float(a[8 * v4 + 5]) * p.scale);
-            w.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * p.scale, __uint_as_float(a[8 * v4 + 7]) * p.scale);
-            reinterpret_cast<uint4*>(dst + ch * 32)[v4] = w;
-          }
-        }
-      }
-    }
-  } else {
-    // ---------------------------------------------------------------- dQ drain, dV
-    const int wq = warp - 4;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    bool ok = true;
-    for (int ii = 0; ii < nq; ++ii) {
-      const int q = (i_first + ii) * kTile + r;
+      // ---- drain dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator
       if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t a[D / 32][32];
+      uint32_t a[D / 64][32];
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(lane_addr + C::S_COL + ch * 32, a[ch]);
+      for (int ch = 0; ch < D / 64; ++ch) tmem_ld32(rs + g * (D / 2) + 32 * ch, a[ch]);
       tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) reg_fence(a[ch]);
+      for (int ch = 0; ch < D / 64; ++ch) reg_fence(a[ch]);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQDRAINED));
+      const int q = q0 + r;
       if (q < sp.seqlen) {
-        float4* dst = reinterpret_cast<float4*>(p.dq_accum + (static_cast<size_t>(sp.row_base) + q) * row_stride +
-                                                static_cast<size_t>(sp.h) * D);
+        const int R = sp.row_base + q;
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch)
+        for (int ch = 0; ch < D / 64; ++ch)
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            atomicAdd(dst + ch * 8 + v,
+            atomicAdd(reinterpret_cast<float4*>(p.dq_accum + dq_index<D>(R, sp.h, p.sv.H, g * (D / 8) + ch * 8 + v)),
                       make_float4(__uint_as_float(a[ch][4 * v]), __uint_as_float(a[ch][4 * v + 1]),
                                   __uint_as_float(a[ch][4 * v + 2]), __uint_as_float(a[ch][4 * v + 3])));
       }
     }
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       tc_fence_after();
-      const int kv_row = kv0 + r;
-      uint16_t* dst = p.dv + (static_cast<size_t>(sp.row_base) + kv_row) * row_stride + static_cast<size_t>(sp.h) * D;
+      const float mul = g == 0 ? p.scale : 1.0f;
+      uint16_t* dst = (g == 0 ? p.dk : p.dv) + (static_cast<size_t>(sp.row_base) + kv_row) * row_stride +
+                      static_cast<size_t>(sp.h) * D;
+      const uint32_t src = lane_addr + (g == 0 ? C::DK_COL : C::DV_COL);
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t a[32];
-        tmem_ld32(lane_addr + C::DV_COL + ch * 32, a);
+        uint32_t v32[32];
+        tmem_ld32(src + ch * 32, v32);
         tmem_wait_ld();
-        reg_fence(a);
-        if (kv_row < sp.seqlen) {
+        reg_fence(v32);
+        if (!row_dead) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1]));
-            w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3]));
-            w.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]), __uint_as_float(a[8 * v4 + 5]));
-            w.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]), __uint_as_float(a[8 * v4 + 7]));
+            w.x = pack_bf16x2(__uint_as_float(v32[8 * v4 + 0]) * mul, __uint_as_float(v32[8 * v4 + 1]) * mul);
+            w.y = pack_bf16x2(__uint_as_float(v32[8 * v4 + 2]) * mul, __uint_as_float(v32[8 * v4 + 3]) * mul);
+            w.z = pack_bf16x2(__uint_as_float(v32[8 * v4 + 4]) * mul, __uint_as_float(v32[8 * v4 + 5]) * mul);
+            w.w = pack_bf16x2(__uint_as_float(v32[8 * v4 + 6]) * mul, __uint_as_float(v32[8 * v4 + 7]) * mul);
             reinterpret_cast<uint4*>(dst + ch * 32)[v4] = w;
           }
         }
@@ -484,8 +539,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess) return e;
-  const size_t n8 = static_cast<size_t>(pairs) * D / 8;
-  fa_bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(p, n8);
+  fa_bwd_post_kernel<D><<<dim3((p.rows + kTile - 1) / kTile, p.sv.H, D / 8), kTile, 0, s>>>(p);
   return cudaGetLastError();
 }
 

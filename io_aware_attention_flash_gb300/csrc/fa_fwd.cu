@@ -286,11 +286,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
             for (int i = 0; i < 32; ++i)
               if (kv0 + ch * 32 + i > lim) s[ch][i] = __float_as_uint(-CUDART_INF_F);
         }
-        float mt = -CUDART_INF_F;
+        // Row max with 8 independent partial maxima (a single running max is a
+        // 128-long dependency chain).
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = -CUDART_INF_F;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(s[ch][i]));
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[ch][i]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 
         if (j == 0) {
           m_ref = mt;
@@ -317,6 +323,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
           }
         }
         const float mc = (m_ref == -CUDART_INF_F) ? 0.f : m_ref * c;
+        float ls[8];  // 8 independent partial row sums
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
@@ -324,11 +333,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e]), c, -mc));
             const float p1 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e + 1]), c, -mc));
-            l += p0 + p1;
+            ls[(2 * e) & 7] += p0;
+            ls[(2 * e + 1) & 7] += p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + ch * 16, pk);
         }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + t));

@@ -75,8 +75,8 @@ def test_fwd_validation(lib):
 
 def test_bwd_validation(lib):
     ws = lib.fa_bwd_workspace_bytes(1, 2, 100, 64)
-    # D: 1*2*100 floats -> 800 -> 1024; dQ accum: 100*2*64*4 = 51200 (already 256-aligned)
-    assert ws == 1024 + 51200
+    # D: 1*2*100 floats -> 800 -> 1024; dQ accum: 100 rows -> 128, 128*2*64*4 = 65536
+    assert ws == 1024 + 65536
 
     def bwd(ws_ptr=FAKE, ws_bytes=ws, d=64, dq=FAKE):
         return lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, ws_ptr, ws_bytes,
@@ -91,7 +91,7 @@ def test_bwd_validation(lib):
 
 def test_varlen_validation(lib):
     ws = lib.fa_bwd_varlen_workspace_bytes(1000, 3, 500, 4, 128)
-    assert ws == (3 * 4 * 500 * 4 + 255) // 256 * 256 + 1000 * 4 * 128 * 4
+    assert ws == (3 * 4 * 500 * 4 + 255) // 256 * 256 + 1024 * 4 * 128 * 4
     f = lib.fa_fwd_varlen
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, NUL, 3, 500, 1000, 4, 128, 0.1, 1, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 500, 1000, 4, 128, 0.1, 1, None) == 4
