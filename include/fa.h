@@ -91,7 +91,7 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
 
 /* Bytes of fp32 workspace fa_bwd needs: D [B, H, N] (padded to 256 bytes)
  * followed by the dQ accumulator, H·d values for each of B·N rows rounded up
- * to a multiple of 128 (an internal tiled layout). */
+ * to a multiple of 128. */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
@@ -169,6 +169,7 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *           2: fp32 FMAs per SM-clock
  *           3: tcgen05.mma bf16 FLOPs per SM-clock, M=128 N=256 K=16, SMEM operands
  *           4: the same with N=128
+ *           5: the same with N=128 and the A operand read from TMEM
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

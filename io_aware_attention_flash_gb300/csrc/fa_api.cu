@@ -126,6 +126,27 @@ fa_status make_map(CUtensorMap* map, const void* ptr, int d, int H, long long ro
   return FA_OK;
 }
 
+// fp32 dQ accumulator [rows, H, d] as a 3-D TMA map (d, H, rows) with a
+// 32-column x 32-row box and 128-byte swizzle: the target of the backward's
+// bulk reduce-adds.  Rows past `rows` are clipped.
+fa_status make_map_dq(CUtensorMap* map, const void* ptr, int d, int H, long long rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled entry point not found", cudaErrorSymbolNotFound);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4};
+  const cuuint32_t box[3] = {32, 1, 32};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(t_detail, sizeof(t_detail), "cuTensorMapEncodeTiled (dQ accumulator) failed (CUresult %d)",
+             static_cast<int>(r));
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 // One-shot kernel timing hook of the calling host thread (fa_set_kernel_events).
 thread_local cudaEvent_t t_main_start = nullptr;
 thread_local cudaEvent_t t_main_end = nullptr;
@@ -228,10 +249,12 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   p.nseq = nseq;
   p.err = err;
   p.timeout_ns = kWaitLimitNs;
+  CUtensorMap tdq;
+  FA_TRY(make_map_dq(&tdq, p.dq_accum, d, H, rows));
   cudaEvent_t ev0 = t_main_start, ev1 = t_main_end;
   t_main_start = t_main_end = nullptr;
   const cudaError_t e =
-      fa::launch_bwd(d, tq, tk, tv, tdo, p, max_seqlen, static_cast<cudaStream_t>(stream), ev0, ev1);
+      fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, max_seqlen, static_cast<cudaStream_t>(stream), ev0, ev1);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
 }
 
@@ -412,7 +435,7 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
   if (!result) return FA_ERR_NULL;
-  if (which < 0 || which > 4 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  if (which < 0 || which > 5 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
   FA_TRY(check_arch());
   uint32_t* err = nullptr;
   FA_TRY(error_word(&err));

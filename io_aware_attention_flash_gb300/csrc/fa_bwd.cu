@@ -17,9 +17,9 @@
 //                  dV_j += Pᵀ dO_i             TMEM(A) x SMEM -> TMEM
 //                  dK_j += dSᵀ Q_i             TMEM(A) x SMEM -> TMEM
 //                  dQ_i  = dS K_j              SMEM(A, MN-major) x SMEM -> TMEM
-//                dQ_i is drained from TMEM by a second warpgroup and added to
-//                the fp32 accumulator with vector atomics (other key tiles add
-//                to the same rows).
+//                dQ_i is drained from TMEM through shared memory and added to
+//                the fp32 accumulator by TMA bulk reduce-adds (other key tiles
+//                add to the same rows).
 //   fa_bwd_post  dQ = bf16(scale · dQ_accum).
 // Warp roles in fa_bwd_main: warps 0-7 (two warpgroups, each owning half of
 // the query columns of a tile; thread r owns key row r = TMEM lane r)
@@ -58,20 +58,6 @@ __device__ __forceinline__ void locate_row(const SeqView& sv, int nseq, int g, i
 }
 
 // ----------------------------------------------------------------------------
-// The fp32 dQ accumulator is tiled by 128 global rows: element (row R, head h,
-// column k) lives at
-//   ((⌊R/128⌋·H + h)·(d/4) + ⌊k/4⌋)·512 + (R mod 128)·4 + (k mod 4)
-// so the 16-byte chunk k/4 of 128 consecutive rows is contiguous.  A warp of
-// the dQ drain (lanes = 32 consecutive query rows, each adding the same column
-// chunk) then touches 512 contiguous bytes per vector atomic instead of 32
-// rows 8 KB apart.
-// ----------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ size_t dq_index(int R, int h, int H, int chunk4) {
-  return ((static_cast<size_t>(R >> 7) * H + h) * (D / 4) + chunk4) * 512 + static_cast<size_t>(R & 127) * 4;
-}
-
-// ----------------------------------------------------------------------------
 // fa_bwd_pre: one warp per (row, head).
 // ----------------------------------------------------------------------------
 template <int D>
@@ -89,13 +75,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
     const uint2 d = *reinterpret_cast<const uint2*>(p.dout + base + lane * 4);
     acc = bf16lo_to_f32(o.x) * bf16lo_to_f32(d.x) + bf16hi_to_f32(o.x) * bf16hi_to_f32(d.x) +
           bf16lo_to_f32(o.y) * bf16lo_to_f32(d.y) + bf16hi_to_f32(o.y) * bf16hi_to_f32(d.y);
-    *reinterpret_cast<float4*>(p.dq_accum + dq_index<D>(g, h, H, lane)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(p.dq_accum + base + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
     const uint32_t o = *reinterpret_cast<const uint32_t*>(p.o + base + lane * 2);
     const uint32_t d = *reinterpret_cast<const uint32_t*>(p.dout + base + lane * 2);
     acc = bf16lo_to_f32(o) * bf16lo_to_f32(d) + bf16hi_to_f32(o) * bf16hi_to_f32(d);
-    *reinterpret_cast<float2*>(p.dq_accum + dq_index<D>(g, h, H, lane >> 1) + (lane & 1) * 2) =
-        make_float2(0.f, 0.f);
+    *reinterpret_cast<float2*>(p.dq_accum + base + lane * 2) = make_float2(0.f, 0.f);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -107,25 +92,20 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
 }
 
 // ----------------------------------------------------------------------------
-// fa_bwd_post: dQ = bf16(scale · accumulator).  Grid (row tiles, H, d/8),
-// 128 threads: thread = row of the tile, 8 columns each (two 16-byte chunks of
-// the tiled accumulator, read coalesced across the block).
+// fa_bwd_post: dQ = bf16(scale · accumulator), 8 elements per thread.
 // ----------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128) fa_bwd_post_kernel(const BwdParams p) {
-  const int R = blockIdx.x * 128 + threadIdx.x;
-  if (R >= p.rows) return;
-  const int h = blockIdx.y, c8 = blockIdx.z;
-  const int H = p.sv.H;
-  const float4 a = *reinterpret_cast<const float4*>(p.dq_accum + dq_index<D>(R, h, H, 2 * c8));
-  const float4 b = *reinterpret_cast<const float4*>(p.dq_accum + dq_index<D>(R, h, H, 2 * c8 + 1));
+__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const BwdParams p, size_t n8) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(p.dq_accum)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(p.dq_accum)[2 * i + 1];
   const float s = p.scale;
   uint4 w;
   w.x = pack_bf16x2(a.x * s, a.y * s);
   w.y = pack_bf16x2(a.z * s, a.w * s);
   w.z = pack_bf16x2(b.x * s, b.y * s);
   w.w = pack_bf16x2(b.z * s, b.w * s);
-  *reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(R) * H + h) * D + 8 * c8) = w;
+  reinterpret_cast<uint4*>(p.dq)[i] = w;
 }
 
 // ----------------------------------------------------------------------------
@@ -186,7 +166,7 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -426,6 +406,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
+      if (lane == 0) bulk_wait_group_read0();  // the dQ_{i-1} reductions have read this warp's slice
+      __syncwarp();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dp[32];
@@ -455,7 +437,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-      // ---- drain dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator
+      // ---- drain dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator.
+      // Each warp stages its 32 rows x 32 columns through its own 4 KB slice of
+      // the dSᵀ tile (free now: dQ_i, its only reader, has completed) in the
+      // 128-byte swizzled layout, and the TMA unit adds the slice into global
+      // memory (one bulk reduce per slice instead of 256 vector atomics).
+      // Rows past the sequence end carry exact zeros (their P, hence dS, is 0).
       if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
@@ -469,18 +456,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       for (int ch = 0; ch < D / 64; ++ch) reg_fence(a[ch]);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQDRAINED));
-      const int q = q0 + r;
-      if (q < sp.seqlen) {
-        const int R = sp.row_base + q;
+      const uint32_t slot = sb + C::OFF_DS + g * C::BLK_BYTES + wq * 4096;
 #pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch)
+      for (int ch = 0; ch < D / 64; ++ch) {
+        if (ch > 0) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+        }
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            atomicAdd(reinterpret_cast<float4*>(p.dq_accum + dq_index<D>(R, sp.h, p.sv.H, g * (D / 8) + ch * 8 + v)),
-                      make_float4(__uint_as_float(a[ch][4 * v]), __uint_as_float(a[ch][4 * v + 1]),
-                                  __uint_as_float(a[ch][4 * v + 2]), __uint_as_float(a[ch][4 * v + 3])));
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t chunk = u ^ (lane & 7);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + lane * 128 + chunk * 16),
+                       "r"(a[ch][4 * u]), "r"(a[ch][4 * u + 1]), "r"(a[ch][4 * u + 2]), "r"(a[ch][4 * u + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tmDQ, slot, g * (D / 2) + 32 * ch, sp.h, sp.row_base + q0 + 32 * wq);
+          bulk_commit_group();
+        }
       }
     }
+    if (lane == 0) bulk_wait_group0();  // reductions complete before the CTA exits
+    __syncwarp();
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
@@ -520,7 +519,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const BwdParams& p, int max_seqlen, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
+                         const CUtensorMap& tdq, const BwdParams& p, int max_seqlen, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = BwdCfg<D>;
   static bool configured = false;
   if (!configured) {
@@ -535,21 +534,22 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   dim3 grid(p.nseq * p.sv.H, (max_seqlen + kTile - 1) / kTile);
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
-  fa_bwd_main_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, tdo, p);
+  fa_bwd_main_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess) return e;
-  fa_bwd_post_kernel<D><<<dim3((p.rows + kTile - 1) / kTile, p.sv.H, D / 8), kTile, 0, s>>>(p);
+  const size_t n8 = static_cast<size_t>(pairs) * D / 8;
+  fa_bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(p, n8);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int max_seqlen, cudaStream_t s,
-                       cudaEvent_t main_start, cudaEvent_t main_end) {
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, max_seqlen, s, main_start, main_end);
-  return launch_bwd_d<128>(tq, tk, tv, tdo, p, max_seqlen, s, main_start, main_end);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
+                       cudaStream_t s, cudaEvent_t main_start, cudaEvent_t main_end) {
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, max_seqlen, s, main_start, main_end);
+  return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, max_seqlen, s, main_start, main_end);
 }
 
 }  // namespace fa

@@ -39,7 +39,7 @@ struct BwdParams {
   const uint16_t* dout;
   const float* lse;
   float* dpsum;           // D = rowsum(dO * O), fp32 [nseq|B, H, lse_stride]
-  float* dq_accum;        // fp32, same layout as q
+  float* dq_accum;        // fp32, same layout as q ([rows, H, d])
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
@@ -81,7 +81,8 @@ __device__ __forceinline__ SeqPos seq_pos(const SeqView& sv) {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int max_seqlen, cudaStream_t s,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
+                       cudaStream_t s,
                        cudaEvent_t main_start = nullptr, cudaEvent_t main_end = nullptr);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s);

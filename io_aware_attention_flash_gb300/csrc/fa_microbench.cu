@@ -52,9 +52,10 @@ __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned 
 }
 
 // tcgen05.mma throughput: one thread issues `iters` x 4 MMAs of M=128, N, K=16
-// (bf16, both operands in shared memory, fp32 accumulate in TMEM) and waits
-// for them to finish.  Operand contents are zero: only the rate matters.
-template <int N>
+// (bf16, fp32 accumulate in TMEM; A from shared memory, or from TMEM when
+// TS) and waits for them to finish.  Operand contents are zero: only the
+// rate matters.
+template <int N, bool TS>
 __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t done_bar;
@@ -78,6 +79,16 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  if (TS) {  // zero the A operand's 32 TMEM columns (128..159), each warp its lane quarter
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, z);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   if (threadIdx.x == 0) {
     constexpr uint32_t idesc = idesc_bf16(128, N, false, false);
     const uint32_t sA = base, sB = base + 128 * 128;
@@ -85,8 +96,11 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
     for (int i = 0; i < iters; ++i) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_ss(tmem, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 32, 16, 1024), idesc,
-               (i | kk) ? 1u : 0u);
+        if (TS)
+          mma_ts(tmem, tmem + 128 + kk * 8, sdesc_sw128(sB + kk * 32, 16, 1024), idesc, (i | kk) ? 1u : 0u);
+        else
+          mma_ss(tmem, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 32, 16, 1024), idesc,
+                 (i | kk) ? 1u : 0u);
     }
     tc_commit(smem_u32(&done_bar));
     wait_drain(smem_u32(&done_bar), 0, err, 2000000000ull);
@@ -101,12 +115,12 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   }
 }
 
-template <int N>
+template <int N, bool TS>
 cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
   const int smem = (128 + N) * 128 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel<N, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mma_rate_kernel<N><<<sms, 128, smem, s>>>(iters, cyc, err);
+  mma_rate_kernel<N, TS><<<sms, 128, smem, s>>>(iters, cyc, err);
   return cudaGetLastError();
 }
 
@@ -130,8 +144,9 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 0: unit_rate_kernel<0><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 1: unit_rate_kernel<1><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 2: unit_rate_kernel<2><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
-    case 3: e = launch_mma_rate<256>(sms, iters, cyc, err, s); break;
-    case 4: e = launch_mma_rate<128>(sms, iters, cyc, err, s); break;
+    case 3: e = launch_mma_rate<256, false>(sms, iters, cyc, err, s); break;
+    case 4: e = launch_mma_rate<128, false>(sms, iters, cyc, err, s); break;
+    case 5: e = launch_mma_rate<128, true>(sms, iters, cyc, err, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
