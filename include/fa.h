@@ -170,6 +170,8 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *           3: tcgen05.mma bf16 FLOPs per SM-clock, M=128 N=256 K=16, SMEM operands
  *           4: the same with N=128
  *           5: the same with N=128 and the A operand read from TMEM
+ *           6, 7: cases 3 and 5 with pseudo-random bf16 operands instead of
+ *              zeros (the data a real GEMM switches, and the power it draws)
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

@@ -51,11 +51,22 @@ __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned 
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// Pseudo-random bf16 pair with magnitudes in [0.5, 1) and random signs.
+__device__ __forceinline__ uint32_t random_bf16x2(uint32_t i) {
+  uint32_t h = i * 0x9E3779B9u;
+  h ^= h >> 15;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  const uint32_t lo = (h & 0x8000u) | 0x3F00u | (h & 0x7Fu);
+  const uint32_t hi = ((h >> 16) & 0x8000u) | 0x3F00u | ((h >> 16) & 0x7Fu);
+  return lo | (hi << 16);
+}
+
 // tcgen05.mma throughput: one thread issues `iters` x 4 MMAs of M=128, N, K=16
 // (bf16, fp32 accumulate in TMEM; A from shared memory, or from TMEM when
-// TS) and waits for them to finish.  Operand contents are zero: only the
-// rate matters.
-template <int N, bool TS>
+// TS) and waits for them to finish.  Operands are zero, or pseudo-random bf16
+// when RND (the realistic case: switching data draws more power than zeros).
+template <int N, bool TS, bool RND>
 __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t done_bar;
@@ -65,7 +76,10 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   uint8_t* gen = smem_raw + (base - raw);
   const int warp = threadIdx.x / 32;
   for (int i = threadIdx.x; i < (128 + N) * 128 / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(gen)[i] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(gen)[i] =
+        RND ? make_uint4(random_bf16x2(4 * i), random_bf16x2(4 * i + 1), random_bf16x2(4 * i + 2),
+                         random_bf16x2(4 * i + 3))
+            : make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&done_bar), 1);
     fence_mbar_init();
@@ -79,10 +93,10 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  if (TS) {  // zero the A operand's 32 TMEM columns (128..159), each warp its lane quarter
+  if (TS) {  // fill the A operand's 32 TMEM columns (128..159), each warp its lane quarter
     uint32_t z[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    for (int i = 0; i < 32; ++i) z[i] = RND ? random_bf16x2(threadIdx.x * 32 + i + 977u) : 0u;
     tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, z);
     tmem_wait_st();
   }
@@ -115,12 +129,13 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   }
 }
 
-template <int N, bool TS>
+template <int N, bool TS, bool RND>
 cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
   const int smem = (128 + N) * 128 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel<N, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(mma_rate_kernel<N, TS, RND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mma_rate_kernel<N, TS><<<sms, 128, smem, s>>>(iters, cyc, err);
+  mma_rate_kernel<N, TS, RND><<<sms, 128, smem, s>>>(iters, cyc, err);
   return cudaGetLastError();
 }
 
@@ -144,16 +159,18 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 0: unit_rate_kernel<0><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 1: unit_rate_kernel<1><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 2: unit_rate_kernel<2><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
-    case 3: e = launch_mma_rate<256, false>(sms, iters, cyc, err, s); break;
-    case 4: e = launch_mma_rate<128, false>(sms, iters, cyc, err, s); break;
-    case 5: e = launch_mma_rate<128, true>(sms, iters, cyc, err, s); break;
+    case 3: e = launch_mma_rate<256, false, false>(sms, iters, cyc, err, s); break;
+    case 4: e = launch_mma_rate<128, false, false>(sms, iters, cyc, err, s); break;
+    case 5: e = launch_mma_rate<128, true, false>(sms, iters, cyc, err, s); break;
+    case 6: e = launch_mma_rate<256, false, true>(sms, iters, cyc, err, s); break;
+    case 7: e = launch_mma_rate<128, true, true>(sms, iters, cyc, err, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   if (which <= 2)
     units_per_cta = static_cast<double>(threads) * iters * kChains;
   else
-    units_per_cta = 2.0 * 128 * (which == 3 ? 256 : 128) * 64 * static_cast<double>(iters);
+    units_per_cta = 2.0 * 128 * ((which == 3 || which == 6) ? 256 : 128) * 64 * static_cast<double>(iters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
   static unsigned long long host_cyc[kMaxSms];

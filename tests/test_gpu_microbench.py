@@ -15,6 +15,8 @@ pytestmark = gpu
     ("mma_bf16_flop_per_sm_clk_n256", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a", 1024, 32768),
+    ("mma_bf16_flop_per_sm_clk_n256_random", 1024, 32768),
+    ("mma_bf16_flop_per_sm_clk_n128_tmem_a_random", 1024, 32768),
 ])
 def test_microbench_rates_plausible(name, lo, hi):
     fa = require_gpu()
