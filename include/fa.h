@@ -172,6 +172,12 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *           5: the same with N=128 and the A operand read from TMEM
  *           6, 7: cases 3 and 5 with pseudo-random bf16 operands instead of
  *              zeros (the data a real GEMM switches, and the power it draws)
+ *           8: bf16 FLOPs per SM-clock of the forward kernel's MMA stream
+ *              alone (two query tiles: O_t += P_t V with P_t from TMEM,
+ *              then S_t = Q K^T over P_t's columns; d = 128)
+ *           9: the same with 64-column O tiles
+ *          10: case 9 with P_t in TMEM columns that no MMA writes
+ *          11: case 8 with both PV MMAs issued before both S MMAs
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

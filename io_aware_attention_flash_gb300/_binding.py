@@ -46,7 +46,10 @@ SIGNATURES = {
 MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk": 2,
               "mma_bf16_flop_per_sm_clk_n256": 3, "mma_bf16_flop_per_sm_clk_n128": 4,
               "mma_bf16_flop_per_sm_clk_n128_tmem_a": 5, "mma_bf16_flop_per_sm_clk_n256_random": 6,
-              "mma_bf16_flop_per_sm_clk_n128_tmem_a_random": 7}
+              "mma_bf16_flop_per_sm_clk_n128_tmem_a_random": 7,
+              "fwd_mma_stream_flop_per_sm_clk_d128": 8, "fwd_mma_stream_flop_per_sm_clk_pv64": 9,
+              "fwd_mma_stream_flop_per_sm_clk_pv64_separate_p": 10,
+              "fwd_mma_stream_flop_per_sm_clk_d128_pv_first": 11}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

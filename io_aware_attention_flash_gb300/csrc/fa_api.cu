@@ -435,7 +435,7 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
   if (!result) return FA_ERR_NULL;
-  if (which < 0 || which > 7 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  if (which < 0 || which > 11 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
   FA_TRY(check_arch());
   uint32_t* err = nullptr;
   FA_TRY(error_word(&err));

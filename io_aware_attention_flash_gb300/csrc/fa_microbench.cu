@@ -139,6 +139,105 @@ cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_
   return cudaGetLastError();
 }
 
+// The forward kernel's MMA stream without its softmax: per iteration and per
+// query tile t, O_t += P_t V (A from TMEM, 8 x K16) then S_t = Q K^T (both
+// from shared memory, 8 x K16), pseudo-random bf16 operands.  TMEM: S_t at
+// columns 128t; with ALIAS the P_t operand lies in S_t's first 64 columns
+// (so each S_t overwrites what the preceding PV_t read), otherwise in
+// columns 384 + 64t that no MMA writes.  SPLIT issues both PVs before both
+// S's.  The rate says how fast the tensor pipe retires this stream when no
+// other unit holds it up.
+template <int DPV, bool ALIAS, bool SPLIT>
+__global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
+  static_assert(ALIAS || DPV == 64, "separate P columns fit only beside 64-column O tiles");
+  constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile: two 128-byte swizzled 64-column blocks
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t tmem_slot;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gen = smem_raw + (base - raw);
+  const int warp = threadIdx.x / 32;
+  for (int i = threadIdx.x; i < 3 * TILE / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gen)[i] =
+        make_uint4(random_bf16x2(4 * i), random_bf16x2(4 * i + 1), random_bf16x2(4 * i + 2), random_bf16x2(4 * i + 3));
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done_bar), 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  {  // pseudo-random bf16 in every column an MMA may read as P before it is written
+    uint32_t z[32];
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c = 0; c < 512; c += 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = random_bf16x2(threadIdx.x * 512 + c + i + 977u);
+      tmem_st32(lane_base + c, z);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16(128, DPV, false, true);
+    const uint32_t sQ = base, sK = base + TILE, sV = base + 2 * TILE;
+    auto s_col = [](int t) -> uint32_t { return 128u * t; };
+    auto o_col = [](int t) -> uint32_t { return 256u + DPV * t; };
+    auto p_col = [](int t) -> uint32_t { return ALIAS ? 128u * t : 384u + 64u * t; };
+    auto pv = [&](int t) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + o_col(t), tmem + p_col(t) + kk * 8, sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idesc_o, 1u);
+    };
+    auto sg = [&](int t) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+        mma_ss(tmem + s_col(t), sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024), idesc_s,
+               kk > 0 ? 1u : 0u);
+      }
+    };
+    const unsigned long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+      if (SPLIT) {
+        pv(0); pv(1); sg(0); sg(1);
+      } else {
+        pv(0); sg(0); pv(1); sg(1);
+      }
+    }
+    tc_commit(smem_u32(&done_bar));
+    wait_drain(smem_u32(&done_bar), 0, err, 2000000000ull);
+    const unsigned long long t1 = clock64();
+    cycles[blockIdx.x] = t1 - t0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DPV, bool ALIAS, bool SPLIT>
+cudaError_t launch_fwd_stream(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
+  const int smem = 3 * 128 * 128 * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<DPV, ALIAS, SPLIT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  fwd_stream_kernel<DPV, ALIAS, SPLIT><<<sms, 128, smem, s>>>(iters, cyc, err);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // Runs one microbenchmark with one CTA per SM and returns the mean over CTAs
@@ -164,13 +263,20 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 5: e = launch_mma_rate<128, true, false>(sms, iters, cyc, err, s); break;
     case 6: e = launch_mma_rate<256, false, true>(sms, iters, cyc, err, s); break;
     case 7: e = launch_mma_rate<128, true, true>(sms, iters, cyc, err, s); break;
+    case 8: e = launch_fwd_stream<128, true, false>(sms, iters, cyc, err, s); break;
+    case 9: e = launch_fwd_stream<64, true, false>(sms, iters, cyc, err, s); break;
+    case 10: e = launch_fwd_stream<64, false, false>(sms, iters, cyc, err, s); break;
+    case 11: e = launch_fwd_stream<128, true, true>(sms, iters, cyc, err, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   if (which <= 2)
     units_per_cta = static_cast<double>(threads) * iters * kChains;
-  else
+  else if (which <= 7)
     units_per_cta = 2.0 * 128 * ((which == 3 || which == 6) ? 256 : 128) * 64 * static_cast<double>(iters);
+  else  // two query tiles x (S: 128 x 128 x 128, PV: 128 x DPV x 128)
+    units_per_cta = 2.0 * (2.0 * 128 * 128 * 128 + 2.0 * 128 * ((which == 9 || which == 10) ? 64 : 128) * 128) *
+                    static_cast<double>(iters);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
   static unsigned long long host_cyc[kMaxSms];

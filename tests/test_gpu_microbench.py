@@ -17,10 +17,14 @@ pytestmark = gpu
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n256_random", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a_random", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_pv64", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_pv64_separate_p", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_pv_first", 1024, 32768),
 ])
 def test_microbench_rates_plausible(name, lo, hi):
     fa = require_gpu()
-    iters = 2048 if name.startswith("mma") else 4096
+    iters = 512 if name.startswith("fwd") else 2048 if name.startswith("mma") else 4096
     rate = fa._binding.fa_microbench(name, iters)
     print(f"{name} = {rate:.2f}")
     assert lo <= rate <= hi
