@@ -82,7 +82,7 @@ def test_backward_full_size_sampled(name):
 
 
 def test_backward_repeatable_and_workspace_reuse():
-    """dQ is accumulated with atomics: results vary only by rounding order;
+    """dQ is accumulated by unordered reduce-adds: results vary only by rounding order;
     a dirty reused workspace must not leak into the result."""
     fa = require_gpu()
     B, N, H, d = 1, 640, 2, 128
