@@ -341,6 +341,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     // ---------------------------------------------------------------- P, dS, dQ drain
     // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ and dQ columns
     // g·d/2 .. (g+1)·d/2-1; thread r of a warpgroup owns TMEM lane r.
+    //
+    // Per query tile i the order is: P_i, the rest of dQ_{i-1}'s drain, dS_i,
+    // then the first part of dQ_i's drain.  P_i (what the tensor core waits
+    // for next) thus follows dQ_{i-1} directly, and the TMA unit reads the
+    // staged dQ slices while P_i is computed instead of in a wait between
+    // them.  The row statistics of tile i+1 are loaded from global memory
+    // during tile i.
+    constexpr int NCH = D / 64;            // 32-column dQ chunks per warp and tile
     const int g = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;          // key row of Sᵀ / dPᵀ; query row of dQ
@@ -348,6 +356,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     const bool row_dead = kv_row >= sp.seqlen;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
+    // This warp's 4 KB slice of the dSᵀ tile: its own dSᵀ rows, and the
+    // staging buffer of its dQ chunks once the dQ GEMM has read dSᵀ.
+    const uint32_t slot = sb + C::OFF_DS + g * C::BLK_BYTES + wq * 4096;
+    auto load_stat = [&](int ii) -> float {
+      const int q = (i_first + ii) * kTile + r;
+      if (q >= sp.seqlen) return g == 0 ? CUDART_INF_F : 0.f;
+      return g == 0 ? __ldg(p.lse + stat_base + q) * kLog2e : __ldg(p.dpsum + stat_base + q);
+    };
+    // Stage one 32 x 32 fp32 chunk (thread = row) into the slot, 128-byte
+    // swizzled, and add it into the accumulator with one TMA bulk reduce.
+    auto drain_chunk = [&](const uint32_t (&v)[32], int ch, int q0c) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t chunk = u ^ (lane & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + lane * 128 + chunk * 16), "r"(v[4 * u]),
+                     "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tmDQ, slot, g * (D / 2) + 32 * ch, sp.h, sp.row_base + q0c + 32 * wq);
+        bulk_commit_group();
+      }
+    };
+    auto slot_read_done = [&]() {
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+    };
+    uint32_t pend[32];                     // dQ_{i-1} chunk 1 (d = 128), drained after P_i
+    float stat_next = nq > 0 ? load_stat(0) : 0.f;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int qi = i_first + ii;
@@ -356,12 +395,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       const uint32_t rp = lane_addr + C::R_COL + ((ii + 1) & 1) * 128;
       float* lse2 = stat + (ii & 1) * 256;
       float* dsum = lse2 + 128;
-      {
-        const int q = q0 + r;
-        const bool valid = q < sp.seqlen;
-        if (g == 0) lse2[r] = valid ? __ldg(p.lse + stat_base + q) * kLog2e : CUDART_INF_F;
-        else dsum[r] = valid ? __ldg(p.dpsum + stat_base + q) : 0.f;
-      }
+      if (g == 0) lse2[r] = stat_next; else dsum[r] = stat_next;
+      if (ii + 1 < nq) stat_next = load_stat(ii + 1);
       // Both warpgroups read all 128 entries: publish them through an mbarrier
       // (a bounded wait, unlike a named barrier, so an abort cannot hang here).
       mbar_arrive(bar(C::B_STAT + (ii & 1)));
@@ -400,14 +435,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::B_PREADY));
+      // ---- the rest of dQ_{i-1}
+      if constexpr (NCH == 2) {
+        if (ii > 0) {
+          slot_read_done();                // chunk 0 of dQ_{i-1} has been read out of the slot
+          drain_chunk(pend, 1, q0 - kTile);
+        }
+      }
       // ---- dSᵀ = Pᵀ ∘ (dPᵀ − D)
       if (!wait_bounded(bar(C::B_DPFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (lane == 0) bulk_wait_group_read0();  // the dQ_{i-1} reductions have read this warp's slice
-      __syncwarp();
+      slot_read_done();                    // dQ_{i-1} is out of the slot that takes this warp's dSᵀ rows
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dp[32];
@@ -437,45 +478,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-      // ---- drain dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator.
-      // Each warp stages its 32 rows x 32 columns through its own 4 KB slice of
-      // the dSᵀ tile (free now: dQ_i, its only reader, has completed) in the
-      // 128-byte swizzled layout, and the TMA unit adds the slice into global
-      // memory (one bulk reduce per slice instead of 256 vector atomics).
+      // ---- dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator.
+      // The slot is free once dQ_i, the only reader of dSᵀ_i, has completed.
       // Rows past the sequence end carry exact zeros (their P, hence dS, is 0).
       if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t a[D / 64][32];
-#pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) tmem_ld32(rs + g * (D / 2) + 32 * ch, a[ch]);
+      uint32_t a0[32];
+      tmem_ld32(rs + g * (D / 2), a0);
+      if constexpr (NCH == 2) tmem_ld32(rs + g * (D / 2) + 32, pend);
       tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) reg_fence(a[ch]);
+      reg_fence(a0);
+      if constexpr (NCH == 2) reg_fence(pend);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQDRAINED));
-      const uint32_t slot = sb + C::OFF_DS + g * C::BLK_BYTES + wq * 4096;
-#pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) {
-        if (ch > 0) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t chunk = u ^ (lane & 7);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + lane * 128 + chunk * 16),
-                       "r"(a[ch][4 * u]), "r"(a[ch][4 * u + 1]), "r"(a[ch][4 * u + 2]), "r"(a[ch][4 * u + 3])
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&tmDQ, slot, g * (D / 2) + 32 * ch, sp.h, sp.row_base + q0 + 32 * wq);
-          bulk_commit_group();
-        }
+      drain_chunk(a0, 0, q0);
+    }
+    if constexpr (NCH == 2) {
+      if (ok && nq > 0) {
+        slot_read_done();
+        drain_chunk(pend, 1, (i_first + nq - 1) * kTile);
       }
     }
     if (lane == 0) bulk_wait_group0();  // reductions complete before the CTA exits

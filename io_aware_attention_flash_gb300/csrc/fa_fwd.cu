@@ -187,21 +187,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+      // Descriptors of the tile bases; each K16 step adds a byte offset.
+      const uint64_t dQ0 = sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, C::BLK_BYTES, 1024);
       auto issue_s = [&](int t, int ks) {
+        const uint64_t dQ = sdesc_add(dQ0, t * C::TILE_BYTES), dK = sdesc_add(dK0, ks * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
-          const uint64_t a = sdesc_sw128(sb + C::OFF_Q + t * C::TILE_BYTES + koff, 16, 1024);
-          const uint64_t b = sdesc_sw128(sb + C::OFF_K + ks * C::TILE_BYTES + koff, 16, 1024);
-          mma_ss(tmem + C::S_COL(t), a, b, idesc_s, kk > 0);
+          mma_ss(tmem + C::S_COL(t), sdesc_add(dQ, koff), sdesc_add(dK, koff), idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int vs, bool acc) {
+        const uint64_t dV = sdesc_add(dV0, vs * C::TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(sb + C::OFF_V + vs * C::TILE_BYTES + kk * 2048, C::BLK_BYTES, 1024);
-          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, sdesc_add(dV, kk * 2048), idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bounded(bar(C::B_Q), 0, abort_flag, p.err, p.timeout_ns) &&
                 wait_bounded(bar(C::B_KFULL + 0), 0, abort_flag, p.err, p.timeout_ns);

@@ -219,6 +219,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          (2ull << 61);    // swizzle mode: 128-byte
 }
 
+// The descriptor of an operand `byte_off` bytes further into shared memory
+// (the start-address field holds address / 16 in 14 bits; shared-memory
+// addresses stay below 2^18, so the add does not carry out of the field).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                   // D format f32
