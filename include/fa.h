@@ -178,6 +178,17 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *           9: the same with 64-column O tiles
  *          10: case 9 with P_t in TMEM columns that no MMA writes
  *          11: case 8 with both PV MMAs issued before both S MMAs
+ *          12: bytes per SM-clock added into a 64 MiB fp32 array by TMA bulk
+ *              reduce-adds of 32 x 32 fp32 chunks, 8 warps per SM, each
+ *              staging its chunks through one 4 KB shared-memory slot (the
+ *              backward's dQ drain); allocates and frees the array on
+ *              `stream`
+ *          13: case 12 with two slots per warp (two reduces in flight)
+ *          14: the same additions as 16-byte vector atomics from registers
+ *              (each lane its own row)
+ *          15: case 14 with the array read as 128-row tiles, so that one
+ *              warp instruction adds 512 contiguous bytes
+ *          16: cases 12 and 15 at once, from half the warps each
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

@@ -49,7 +49,10 @@ MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk"
               "mma_bf16_flop_per_sm_clk_n128_tmem_a_random": 7,
               "fwd_mma_stream_flop_per_sm_clk_d128": 8, "fwd_mma_stream_flop_per_sm_clk_pv64": 9,
               "fwd_mma_stream_flop_per_sm_clk_pv64_separate_p": 10,
-              "fwd_mma_stream_flop_per_sm_clk_d128_pv_first": 11}
+              "fwd_mma_stream_flop_per_sm_clk_d128_pv_first": 11,
+              "tma_reduce_bytes_per_sm_clk": 12, "tma_reduce_bytes_per_sm_clk_2slots": 13,
+              "red_v4_bytes_per_sm_clk": 14, "red_v4_coalesced_bytes_per_sm_clk": 15,
+              "tma_and_red_v4_bytes_per_sm_clk": 16}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

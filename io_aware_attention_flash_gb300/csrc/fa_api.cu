@@ -435,8 +435,29 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
   if (!result) return FA_ERR_NULL;
-  if (which < 0 || which > 11 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  if (which < 0 || which > 16 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
   FA_TRY(check_arch());
+  if (which >= 12) {
+    // Reduce-add throughput into a 64 MiB fp32 array shaped [8192, 16, 128].
+    constexpr int rows = 8192;
+    const size_t bytes = static_cast<size_t>(rows) * 16 * 128 * 4;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* buf = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&buf), bytes, s);
+    if (e != cudaSuccess) return cuda_fail("microbenchmark buffer", e);
+    fa_status st = FA_OK;
+    if ((e = cudaMemsetAsync(buf, 0, bytes, s)) != cudaSuccess) {
+      st = cuda_fail("microbenchmark buffer", e);
+    } else {
+      CUtensorMap tm;
+      st = make_map_dq(&tm, buf, 128, 16, rows);
+      if (st == FA_OK && (e = fa::run_reduce_microbench(which, iters, tm, buf, rows, result, s)) != cudaSuccess)
+        st = cuda_fail("microbenchmark", e);
+    }
+    const cudaError_t ef = cudaFreeAsync(buf, s);
+    if (st == FA_OK && ef != cudaSuccess) st = cuda_fail("microbenchmark buffer", ef);
+    return st;
+  }
   uint32_t* err = nullptr;
   FA_TRY(error_word(&err));
   const cudaError_t e = fa::run_microbench(which, iters, err, result, static_cast<cudaStream_t>(stream));

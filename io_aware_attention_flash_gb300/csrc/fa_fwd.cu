@@ -289,17 +289,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
             for (int i = 0; i < 32; ++i)
               if (kv0 + ch * 32 + i > lim) s[ch][i] = __float_as_uint(-CUDART_INF_F);
         }
-        // Row max with 8 independent partial maxima (a single running max is a
-        // 128-long dependency chain).
-        float mx[8];
+        // Row max: three-input max into 4 independent partial maxima (a single
+        // running max is a long dependency chain).
+        float mx[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = -CUDART_INF_F;
+        for (int k = 0; k < 4; ++k) mx[k] = -CUDART_INF_F;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[ch][i]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int i = 0; i < 16; ++i)
+            mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(s[ch][2 * i]), __uint_as_float(s[ch][2 * i + 1]));
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 
         if (j == 0) {
           m_ref = mt;
@@ -326,22 +326,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
           }
         }
         const float mc = (m_ref == -CUDART_INF_F) ? 0.f : m_ref * c;
-        float ls[8];  // 8 independent partial row sums
+        // Column pairs go through the paired fp32 instructions: c·s − c·m for
+        // two columns per FMA, and 4 paired partial row sums (the same 8
+        // partial sums, in the same order, as one sum per column mod 8).
+        const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+        uint64_t ls2[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+        for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e]), c, -mc));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e + 1]), c, -mc));
-            ls[(2 * e) & 7] += p0;
-            ls[(2 * e + 1) & 7] += p1;
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(s[ch][2 * e]), __uint_as_float(s[ch][2 * e + 1])), c2, nmc2), x0,
+                      x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            ls2[e & 3] = fadd2(ls2[e & 3], f2_pack(p0, p1));
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + ch * 16, pk);
         }
+        float ls[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
         tc_fence_before();

@@ -86,5 +86,7 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        cudaEvent_t main_start = nullptr, cudaEvent_t main_end = nullptr);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s);
+cudaError_t run_reduce_microbench(int which, int iters, const CUtensorMap& tm, float* buf, int rows, double* result,
+                                  cudaStream_t s);
 
 }  // namespace fa

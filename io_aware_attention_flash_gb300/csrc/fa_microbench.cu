@@ -238,6 +238,96 @@ cudaError_t launch_fwd_stream(int sms, int iters, unsigned long long* cyc, uint3
   return cudaGetLastError();
 }
 
+// Reduce-add throughput into a global fp32 array shaped like the backward's
+// dQ accumulator ([rows, 16, 128]), from a CTA of 8 warps per SM.  Each warp
+// repeatedly adds a 32-row x 32-column fp32 chunk at a pseudo-random place:
+//   VIA_TMA: stages the chunk in its own 4 KB shared-memory slot (NSLOT slots
+//            per warp, used in turn) and issues one TMA bulk reduce-add, as
+//            the backward's dQ drain does;
+//   MODE 1:  each lane adds its row's 128 bytes from registers with eight
+//            16-byte vector atomics (a warp instruction touches 32 rows);
+//   MODE 2:  the same atomics laid out so that one warp instruction covers
+//            512 contiguous bytes (the array read as 128-row tiles, a 16-byte
+//            column chunk of 128 consecutive rows stored together);
+//   MODE 3:  warps 0-3 as VIA_TMA, warps 4-7 as MODE 2 (both paths at once).
+// Reports bytes added per SM per clock.
+template <bool VIA_TMA, int NSLOT, int MODE = 0>
+__global__ void __launch_bounds__(256, 1)
+    reduce_rate_kernel(const __grid_constant__ CUtensorMap tm, float* buf, int rows, int iters,
+                       unsigned long long* cycles) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int ntile = rows / 32;
+  uint32_t v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(1e-7f * (lane + i));
+  __syncthreads();
+  const unsigned long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+    const int c0 = 32 * (warp & 3);
+    const int h = (blockIdx.x + it) & 15;
+    const int row = ((blockIdx.x * 131 + it * 7 + (warp >> 2) * 3) % ntile) * 32;
+    const bool use_tma = VIA_TMA || (MODE == 3 && warp < 4);
+    if (use_tma) {
+      const uint32_t slot = base + (warp * NSLOT + it % NSLOT) * 4096;
+      if (it >= NSLOT) {
+        if (lane == 0) bulk_wait_group_read<NSLOT - 1>();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t chunk = u ^ (lane & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + lane * 128 + chunk * 16), "r"(v[4 * u]),
+                     "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tm, slot, c0, h, row);
+        bulk_commit_group();
+      }
+    } else if (MODE == 1) {
+      float* dst = buf + (static_cast<size_t>(row + lane) * 16 + h) * 128 + c0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        atomicAdd(reinterpret_cast<float4*>(dst + 4 * u),
+                  make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                              __uint_as_float(v[4 * u + 3])));
+    } else {
+      // 128-row tile (row / 128, h), 16-byte column chunk k: 128 rows x 16 B contiguous
+      const int R = row + lane;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = c0 / 4 + u;
+        float* dst = buf + ((static_cast<size_t>(R >> 7) * 16 + h) * 32 + k) * 512 + (R & 127) * 4;
+        atomicAdd(reinterpret_cast<float4*>(dst),
+                  make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                              __uint_as_float(v[4 * u + 3])));
+      }
+    }
+  }
+  if (VIA_TMA || MODE == 3) {
+    if (lane == 0) bulk_wait_group0();
+  }
+  __syncthreads();
+  const unsigned long long t1 = clock64();
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+template <bool VIA_TMA, int NSLOT, int MODE = 0>
+cudaError_t launch_reduce_rate(int sms, const CUtensorMap& tm, float* buf, int rows, int iters,
+                               unsigned long long* cyc, cudaStream_t s) {
+  const int smem = (VIA_TMA || MODE == 3) ? 8 * NSLOT * 4096 + 1024 : 0;
+  cudaError_t e = cudaFuncSetAttribute(reduce_rate_kernel<VIA_TMA, NSLOT, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  reduce_rate_kernel<VIA_TMA, NSLOT, MODE><<<sms, 256, smem, s>>>(tm, buf, rows, iters, cyc);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // Runs one microbenchmark with one CTA per SM and returns the mean over CTAs
@@ -284,6 +374,40 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     return e;
   double acc = 0;
   for (int i = 0; i < sms; ++i) acc += units_per_cta / static_cast<double>(host_cyc[i] ? host_cyc[i] : 1);
+  *result = acc / sms;
+  return cudaSuccess;
+}
+
+// Reduce-add throughput (see reduce_rate_kernel); `tm` maps `buf` as
+// [rows, 16, 128] fp32 with a 32 x 1 x 32 box.  which = 12: TMA, one slot per
+// warp; 13: TMA, two slots per warp; 14: vector atomics, 32 rows per warp
+// instruction; 15: vector atomics, 512 contiguous bytes per warp instruction;
+// 16: TMA and contiguous atomics from half the warps each.
+cudaError_t run_reduce_microbench(int which, int iters, const CUtensorMap& tm, float* buf, int rows, double* result,
+                                  cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (sms > kMaxSms) sms = kMaxSms;
+  unsigned long long* cyc = nullptr;
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&cyc), g_cycles)) != cudaSuccess) return e;
+  switch (which) {
+    case 12: e = launch_reduce_rate<true, 1>(sms, tm, buf, rows, iters, cyc, s); break;
+    case 13: e = launch_reduce_rate<true, 2>(sms, tm, buf, rows, iters, cyc, s); break;
+    case 14: e = launch_reduce_rate<false, 1, 1>(sms, tm, buf, rows, iters, cyc, s); break;
+    case 15: e = launch_reduce_rate<false, 1, 2>(sms, tm, buf, rows, iters, cyc, s); break;
+    case 16: e = launch_reduce_rate<false, 1, 3>(sms, tm, buf, rows, iters, cyc, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  static unsigned long long host_cyc[kMaxSms];
+  if ((e = cudaMemcpy(host_cyc, cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return e;
+  const double bytes_per_cta = 8.0 * 4096.0 * iters;
+  double acc = 0;
+  for (int i = 0; i < sms; ++i) acc += bytes_per_cta / static_cast<double>(host_cyc[i] ? host_cyc[i] : 1);
   *result = acc / sms;
   return cudaSuccess;
 }

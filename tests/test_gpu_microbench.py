@@ -21,10 +21,15 @@ pytestmark = gpu
     ("fwd_mma_stream_flop_per_sm_clk_pv64", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_pv64_separate_p", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_d128_pv_first", 1024, 32768),
+    ("tma_reduce_bytes_per_sm_clk", 0.5, 256),
+    ("tma_reduce_bytes_per_sm_clk_2slots", 0.5, 256),
+    ("red_v4_bytes_per_sm_clk", 0.5, 256),
+    ("red_v4_coalesced_bytes_per_sm_clk", 0.5, 256),
+    ("tma_and_red_v4_bytes_per_sm_clk", 0.5, 256),
 ])
 def test_microbench_rates_plausible(name, lo, hi):
     fa = require_gpu()
-    iters = 512 if name.startswith("fwd") else 2048 if name.startswith("mma") else 4096
+    iters = 512 if name.startswith(("fwd", "tma", "red")) else 2048 if name.startswith("mma") else 4096
     rate = fa._binding.fa_microbench(name, iters)
     print(f"{name} = {rate:.2f}")
     assert lo <= rate <= hi
