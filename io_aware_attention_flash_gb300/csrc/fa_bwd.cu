@@ -136,8 +136,10 @@ struct BwdCfg {
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;
   static constexpr int B_DOFULL = B_QFULL + NSQ;
-  static constexpr int B_QEMPTY = B_DOFULL + NSQ;
-  static constexpr int B_SFULL = B_QEMPTY + NSQ;
+  // B_STAGED[s]: the compute warps have staged the dQ of the query tile in
+  // ring slot s over that tile's (consumed) Q and dO.
+  static constexpr int B_STAGED = B_DOFULL + NSQ;
+  static constexpr int B_SFULL = B_STAGED + NSQ;
   static constexpr int B_DPFULL = B_SFULL + 1;
   static constexpr int B_PREADY = B_DPFULL + 1;
   static constexpr int B_DSREADY = B_PREADY + 1;
@@ -151,6 +153,14 @@ struct BwdCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // Whatever is left of the 227 KB opt-in limit is alignment slack.
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
+  static constexpr int NCH = D / 64;                   // 32-column dQ chunks per compute warp
+  // Staging slice of compute warp (g, wq), chunk ch, for the tile in ring
+  // slot qs: the tile's Q (chunk 0) and dO (chunk 1) regions, 4 KB per warp;
+  // with d = 64 (one chunk), warpgroup 0 uses Q and warpgroup 1 dO.
+  __host__ __device__ static constexpr uint32_t dq_slot(int qs, int g, int wq, int ch) {
+    return NCH == 2 ? (ch == 0 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + (g * 4 + wq) * 4096
+                    : (g == 0 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + wq * 4096;
+  }
   static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
   static constexpr int NUM_THREADS = NUM_COMPUTE + 64;
   static constexpr int PRODUCER_WARP = 8;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     for (int s = 0; s < C::NSQ; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1);
       mbar_init(bar(C::B_DOFULL + s), 1);
-      mbar_init(bar(C::B_QEMPTY + s), 1);
+      mbar_init(bar(C::B_STAGED + s), C::NUM_COMPUTE);
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
@@ -238,13 +248,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
                     sp.tma_b);
       }
+      // The dQ of query tile t is staged (fp32, 128-byte swizzled, one 4 KB
+      // slice per compute warp and 32-column chunk) over Q_t and dO_t in
+      // ring slot t % NSQ once the MMAs have consumed them.  This thread adds
+      // the slices into the accumulator with TMA bulk reduce-adds and reuses
+      // the slot for tile t + NSQ once the reduces have read it.
+      auto reduce_tile = [&](int t) -> bool {
+        const int qs = t % C::NSQ;
+        if (!wait_bounded(bar(C::B_STAGED + qs), (t / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+        const int q0 = (i_first + t) * kTile;
+#pragma unroll 1
+        for (int w = 0; w < 8; ++w) {
+          const int g = w >> 2, wq = w & 3;
+#pragma unroll
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_reduce_add_3d(&tmDQ, sb + C::dq_slot(qs, g, wq, ch), g * (D / 2) + 32 * ch, sp.h,
+                              sp.row_base + q0 + 32 * wq);
+        }
+        bulk_commit_group();
+        return true;
+      };
       int fills = 0;
       for (int ii = 0; ii < nq; ++ii) {
         const int qs = ii % C::NSQ;
         const int qrow = sp.tma_row0 + (i_first + ii) * kTile;
-        if (ii >= C::NSQ && !wait_bounded(bar(C::B_QEMPTY + qs), ((ii / C::NSQ) - 1) & 1, abort_flag, p.err,
-                                          p.timeout_ns))
-          break;
+        if (ii >= C::NSQ) {
+          if (!reduce_tile(ii - C::NSQ)) break;
+          bulk_wait_group_read0();   // the slot's staged dQ has been read
+        }
         mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE_BYTES);
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_4d(sb + C::OFF_Q + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_QFULL + qs),
@@ -255,6 +286,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                       kb * 64, sp.h, qrow, sp.tma_b);
         ++fills;
       }
+      if (!*abort_flag) {
+        for (int t = (nq > C::NSQ ? nq - C::NSQ : 0); t < nq; ++t)
+          if (!reduce_tile(t)) break;
+      }
+      bulk_wait_group0();   // every reduce has completed before the CTA exits
       if (*abort_flag) {
         wait_drain(bar(C::B_KV), 0, p.err, p.timeout_ns);
         for (int s = 0; s < C::NSQ && s < fills; ++s) {
@@ -271,50 +307,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);      // dV, dK (A from TMEM)
       constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);        // dQ (A = dS, MN-major)
       auto region = [&](int r) -> uint32_t { return tmem + C::R_COL + (r & 1) * 128; };
-      auto issue_sp = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+      // Tile-base descriptors, K-major (k steps of 32 bytes within a
+      // 128-byte row) and MN-major (k steps of 16 rows = 2048 bytes).
+      const uint64_t kmK = sdesc_sw128(sb + C::OFF_K, 16, 1024), kmV = sdesc_sw128(sb + C::OFF_V, 16, 1024);
+      const uint64_t kmQ = sdesc_sw128(sb + C::OFF_Q, 16, 1024), kmDO = sdesc_sw128(sb + C::OFF_DO, 16, 1024);
+      const uint64_t mnQ = sdesc_sw128(sb + C::OFF_Q, C::BLK_BYTES, 1024);
+      const uint64_t mnDO = sdesc_sw128(sb + C::OFF_DO, C::BLK_BYTES, 1024);
+      const uint64_t mnK = sdesc_sw128(sb + C::OFF_K, C::BLK_BYTES, 1024);
+      const uint64_t mnDS = sdesc_sw128(sb + C::OFF_DS, C::BLK_BYTES, 1024);
+      auto issue_sp = [&](uint32_t dst, uint64_t a, uint64_t b) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
-          mma_ss(dst, sdesc_sw128(a_base + koff, 16, 1024), sdesc_sw128(b_base + koff, 16, 1024), idesc_sp, kk > 0);
+          mma_ss(dst, sdesc_add(a, koff), sdesc_add(b, koff), idesc_sp, kk > 0);
         }
       };
       bool ok = wait_bounded(bar(C::B_KV), 0, abort_flag, p.err, p.timeout_ns) &&
                 wait_bounded(bar(C::B_QFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       if (ok) {
         tc_fence_after();
-        issue_sp(region(0), sb + C::OFF_K, sb + C::OFF_Q);                 // Sᵀ_0 -> R0
+        issue_sp(region(0), kmK, kmQ);                                     // Sᵀ_0 -> R0
         tc_commit(bar(C::B_SFULL));
         ok = wait_bounded(bar(C::B_DOFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       }
       if (ok) {
         tc_fence_after();
-        issue_sp(region(1), sb + C::OFF_V, sb + C::OFF_DO);                // dPᵀ_0 -> R1
+        issue_sp(region(1), kmV, kmDO);                                    // dPᵀ_0 -> R1
         tc_commit(bar(C::B_DPFULL));
       }
       for (int ii = 0; ok && ii < nq; ++ii) {
         const int qs = ii % C::NSQ;
-        const uint32_t sQ = sb + C::OFF_Q + qs * C::TILE_BYTES;
-        const uint32_t sdO = sb + C::OFF_DO + qs * C::TILE_BYTES;
+        const uint64_t bQ = sdesc_add(mnQ, qs * C::TILE_BYTES), bdO = sdesc_add(mnDO, qs * C::TILE_BYTES);
         const uint32_t rs = region(ii), rp = region(ii + 1);
         ok = wait_bounded(bar(C::B_PREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)  // dV += Pᵀ dO_i (Pᵀ packed in rs)
-          mma_ts(tmem + C::DV_COL, rs + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(sdO + kk * 2048, C::BLK_BYTES, 1024), idesc_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, rs + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bdO, kk * 2048), idesc_kv,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
         ok = wait_bounded(bar(C::B_DSREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dSᵀ Q_i (dSᵀ packed in rp)
-          mma_ts(tmem + C::DK_COL, rp + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(sQ + kk * 2048, C::BLK_BYTES, 1024), idesc_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_QEMPTY + qs));
+          mma_ts(tmem + C::DK_COL, rp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bQ, kk * 2048), idesc_kv,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)  // dQ_i = dS K_j -> rs
-          mma_ss(rs, sdesc_sw128(sb + C::OFF_DS + kk * 2048, C::BLK_BYTES, 1024),
-                 sdesc_sw128(sb + C::OFF_K + kk * 2048, C::BLK_BYTES, 1024), idesc_q, kk > 0);
+          mma_ss(rs, sdesc_add(mnDS, kk * 2048), sdesc_add(mnK, kk * 2048), idesc_q, kk > 0);
         tc_commit(bar(C::B_DQFULL));
         if (ii + 1 < nq) {
           const int qs1 = (ii + 1) % C::NSQ;
@@ -322,14 +363,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
           ok = wait_bounded(bar(C::B_QFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          issue_sp(rp, sb + C::OFF_K, sb + C::OFF_Q + qs1 * C::TILE_BYTES);     // Sᵀ_{i+1} -> rp
+          issue_sp(rp, kmK, sdesc_add(kmQ, qs1 * C::TILE_BYTES));               // Sᵀ_{i+1} -> rp
           tc_commit(bar(C::B_SFULL));
           ok = wait_bounded(bar(C::B_DQDRAINED), ii & 1, abort_flag, p.err, p.timeout_ns);
           if (!ok) break;
           ok = wait_bounded(bar(C::B_DOFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          issue_sp(rs, sb + C::OFF_V, sb + C::OFF_DO + qs1 * C::TILE_BYTES);    // dPᵀ_{i+1} -> rs
+          issue_sp(rs, kmV, sdesc_add(kmDO, qs1 * C::TILE_BYTES));              // dPᵀ_{i+1} -> rs
           tc_commit(bar(C::B_DPFULL));
         }
       }
@@ -342,13 +383,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ and dQ columns
     // g·d/2 .. (g+1)·d/2-1; thread r of a warpgroup owns TMEM lane r.
     //
-    // Per query tile i the order is: P_i, the rest of dQ_{i-1}'s drain, dS_i,
-    // then the first part of dQ_i's drain.  P_i (what the tensor core waits
-    // for next) thus follows dQ_{i-1} directly, and the TMA unit reads the
-    // staged dQ slices while P_i is computed instead of in a wait between
-    // them.  The row statistics of tile i+1 are loaded from global memory
-    // during tile i.
-    constexpr int NCH = D / 64;            // 32-column dQ chunks per warp and tile
+    // Per query tile i: P_i, dS_i, then dQ_i is staged over the tile's
+    // consumed Q_i / dO_i ring slot (the TMA producer adds it into the
+    // accumulator), so these warps never wait for the TMA unit.  The row
+    // statistics of tile i+1 are loaded from global memory during tile i.
+    constexpr int NCH = C::NCH;
     const int g = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;          // key row of Sᵀ / dPᵀ; query row of dQ
@@ -356,36 +395,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     const bool row_dead = kv_row >= sp.seqlen;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
-    // This warp's 4 KB slice of the dSᵀ tile: its own dSᵀ rows, and the
-    // staging buffer of its dQ chunks once the dQ GEMM has read dSᵀ.
-    const uint32_t slot = sb + C::OFF_DS + g * C::BLK_BYTES + wq * 4096;
     auto load_stat = [&](int ii) -> float {
       const int q = (i_first + ii) * kTile + r;
       if (q >= sp.seqlen) return g == 0 ? CUDART_INF_F : 0.f;
       return g == 0 ? __ldg(p.lse + stat_base + q) * kLog2e : __ldg(p.dpsum + stat_base + q);
     };
-    // Stage one 32 x 32 fp32 chunk (thread = row) into the slot, 128-byte
-    // swizzled, and add it into the accumulator with one TMA bulk reduce.
-    auto drain_chunk = [&](const uint32_t (&v)[32], int ch, int q0c) {
+    // Stage one 32 x 32 fp32 chunk (thread = row) into a 4 KB slice,
+    // 128-byte swizzled (the layout of the accumulator map's box).
+    auto stage_chunk = [&](const uint32_t (&v)[32], uint32_t slice) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint32_t chunk = u ^ (lane & 7);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + lane * 128 + chunk * 16), "r"(v[4 * u]),
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slice + lane * 128 + chunk * 16), "r"(v[4 * u]),
                      "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
                      : "memory");
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(&tmDQ, slot, g * (D / 2) + 32 * ch, sp.h, sp.row_base + q0c + 32 * wq);
-        bulk_commit_group();
-      }
     };
-    auto slot_read_done = [&]() {
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
-    };
-    uint32_t pend[32];                     // dQ_{i-1} chunk 1 (d = 128), drained after P_i
     float stat_next = nq > 0 ? load_stat(0) : 0.f;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
@@ -435,20 +460,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::B_PREADY));
-      // ---- the rest of dQ_{i-1}
-      if constexpr (NCH == 2) {
-        if (ii > 0) {
-          slot_read_done();                // chunk 0 of dQ_{i-1} has been read out of the slot
-          drain_chunk(pend, 1, q0 - kTile);
-        }
-      }
       // ---- dSᵀ = Pᵀ ∘ (dPᵀ − D)
       if (!wait_bounded(bar(C::B_DPFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      slot_read_done();                    // dQ_{i-1} is out of the slot that takes this warp's dSᵀ rows
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dp[32];
@@ -478,32 +495,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-      // ---- dQ_i (query row r, columns g·d/2 ..) into the fp32 accumulator.
-      // The slot is free once dQ_i, the only reader of dSᵀ_i, has completed.
+      // ---- dQ_i (query row r, columns g·d/2 ..): stage it over Q_i / dO_i,
+      // free once every MMA of tile i (the last is dQ_i) has completed.
       // Rows past the sequence end carry exact zeros (their P, hence dS, is 0).
       if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t a0[32];
-      tmem_ld32(rs + g * (D / 2), a0);
-      if constexpr (NCH == 2) tmem_ld32(rs + g * (D / 2) + 32, pend);
+      uint32_t a[NCH][32];
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(rs + g * (D / 2) + 32 * ch, a[ch]);
       tmem_wait_ld();
-      reg_fence(a0);
-      if constexpr (NCH == 2) reg_fence(pend);
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) reg_fence(a[ch]);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQDRAINED));
-      drain_chunk(a0, 0, q0);
+      const int qs = ii % C::NSQ;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) stage_chunk(a[ch], sb + C::dq_slot(qs, g, wq, ch));
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_STAGED + qs));
     }
-    if constexpr (NCH == 2) {
-      if (ok && nq > 0) {
-        slot_read_done();
-        drain_chunk(pend, 1, (i_first + nq - 1) * kTile);
-      }
-    }
-    if (lane == 0) bulk_wait_group0();  // reductions complete before the CTA exits
-    __syncwarp();
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
