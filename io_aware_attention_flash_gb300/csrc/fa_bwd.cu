@@ -136,7 +136,7 @@ struct BwdCfg {
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;
   static constexpr int B_DOFULL = B_QFULL + NSQ;
-  // B_STAGED[s]: the compute warps have staged the dQ of the query tile in
+  // B_STAGED[s]: the drain warps have staged the dQ of the query tile in
   // ring slot s over that tile's (consumed) Q and dO.
   static constexpr int B_STAGED = B_DOFULL + NSQ;
   static constexpr int B_SFULL = B_STAGED + NSQ;
@@ -153,18 +153,19 @@ struct BwdCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // Whatever is left of the 227 KB opt-in limit is alignment slack.
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
-  static constexpr int NCH = D / 64;                   // 32-column dQ chunks per compute warp
-  // Staging slice of compute warp (g, wq), chunk ch, for the tile in ring
-  // slot qs: the tile's Q (chunk 0) and dO (chunk 1) regions, 4 KB per warp;
-  // with d = 64 (one chunk), warpgroup 0 uses Q and warpgroup 1 dO.
-  __host__ __device__ static constexpr uint32_t dq_slot(int qs, int g, int wq, int ch) {
-    return NCH == 2 ? (ch == 0 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + (g * 4 + wq) * 4096
-                    : (g == 0 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + wq * 4096;
+  static constexpr int NCHT = D / 32;                  // 32-column dQ chunks per row
+  // Staging slice (32 rows x 32 fp32 columns, 4 KB) of dQ rows 32·wq .. +31,
+  // columns 32·c .. +31, for the tile in ring slot qs: the first half of the
+  // chunks over the tile's Q, the second half over its dO.
+  __host__ __device__ static constexpr uint32_t dq_slot(int qs, int c, int wq) {
+    return (c < NCHT / 2 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + ((c % (NCHT / 2)) * 4 + wq) * 4096;
   }
   static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
-  static constexpr int NUM_THREADS = NUM_COMPUTE + 64;
+  static constexpr int NUM_DRAIN = 128;                // warps 10-13: one per TMEM lane quarter
+  static constexpr int NUM_THREADS = NUM_COMPUTE + 64 + NUM_DRAIN;
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
+  static constexpr int DRAIN_WARP0 = 10;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0;
   static constexpr uint32_t DK_COL = D;
@@ -207,14 +208,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     for (int s = 0; s < C::NSQ; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1);
       mbar_init(bar(C::B_DOFULL + s), 1);
-      mbar_init(bar(C::B_STAGED + s), C::NUM_COMPUTE);
+      mbar_init(bar(C::B_STAGED + s), C::NUM_DRAIN);
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PREADY), C::NUM_COMPUTE);
     mbar_init(bar(C::B_DSREADY), C::NUM_COMPUTE);
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQDRAINED), C::NUM_COMPUTE);
+    mbar_init(bar(C::B_DQDRAINED), C::NUM_DRAIN);
     mbar_init(bar(C::B_DKDV), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_STAT + 0), C::NUM_COMPUTE);
@@ -249,8 +250,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                     sp.tma_b);
       }
       // The dQ of query tile t is staged (fp32, 128-byte swizzled, one 4 KB
-      // slice per compute warp and 32-column chunk) over Q_t and dO_t in
-      // ring slot t % NSQ once the MMAs have consumed them.  This thread adds
+      // slice per 32 rows and 32 columns) over Q_t and dO_t in ring slot
+      // t % NSQ once the MMAs have consumed them.  This thread adds
       // the slices into the accumulator with TMA bulk reduce-adds and reuses
       // the slot for tile t + NSQ once the reduces have read it.
       auto reduce_tile = [&](int t) -> bool {
@@ -258,12 +259,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         if (!wait_bounded(bar(C::B_STAGED + qs), (t / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) return false;
         const int q0 = (i_first + t) * kTile;
 #pragma unroll 1
-        for (int w = 0; w < 8; ++w) {
-          const int g = w >> 2, wq = w & 3;
+        for (int wq = 0; wq < 4; ++wq) {
 #pragma unroll
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_reduce_add_3d(&tmDQ, sb + C::dq_slot(qs, g, wq, ch), g * (D / 2) + 32 * ch, sp.h,
-                              sp.row_base + q0 + 32 * wq);
+          for (int c = 0; c < C::NCHT; ++c)
+            tma_reduce_add_3d(&tmDQ, sb + C::dq_slot(qs, c, wq), 32 * c, sp.h, sp.row_base + q0 + 32 * wq);
         }
         bulk_commit_group();
         return true;
@@ -378,30 +377,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       tc_commit(bar(C::B_DRAIN));
       wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
     }
-  } else {
-    // ---------------------------------------------------------------- P, dS, dQ drain
-    // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ and dQ columns
-    // g·d/2 .. (g+1)·d/2-1; thread r of a warpgroup owns TMEM lane r.
-    //
-    // Per query tile i: P_i, dS_i, then dQ_i is staged over the tile's
-    // consumed Q_i / dO_i ring slot (the TMA producer adds it into the
-    // accumulator), so these warps never wait for the TMA unit.  The row
-    // statistics of tile i+1 are loaded from global memory during tile i.
-    constexpr int NCH = C::NCH;
-    const int g = warp >> 2;
+  } else if (warp >= C::DRAIN_WARP0) {
+    // ---------------------------------------------------------------- dQ drain
+    // One warp per TMEM lane quarter wq (dQ rows 32·wq .. +31 of the query
+    // tile; thread = row).  Once dQ_i has completed, copy the rows from TMEM
+    // into the 128-byte swizzled staging slices over Q_i / dO_i, two 32-column
+    // chunks at a time, release the TMEM region to the MMA warp and hand the
+    // slices to the TMA producer, which adds them into the accumulator.  Rows
+    // past the sequence end carry exact zeros (their P, hence dS, is 0).
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;          // key row of Sᵀ / dPᵀ; query row of dQ
-    const int kv_row = kv0 + r;
-    const bool row_dead = kv_row >= sp.seqlen;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const float c = p.scale_log2;
-    auto load_stat = [&](int ii) -> float {
-      const int q = (i_first + ii) * kTile + r;
-      if (q >= sp.seqlen) return g == 0 ? CUDART_INF_F : 0.f;
-      return g == 0 ? __ldg(p.lse + stat_base + q) * kLog2e : __ldg(p.dpsum + stat_base + q);
-    };
-    // Stage one 32 x 32 fp32 chunk (thread = row) into a 4 KB slice,
-    // 128-byte swizzled (the layout of the accumulator map's box).
     auto stage_chunk = [&](const uint32_t (&v)[32], uint32_t slice) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -411,20 +396,67 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                      : "memory");
       }
     };
-    float stat_next = nq > 0 ? load_stat(0) : 0.f;
+    for (int ii = 0; ii < nq; ++ii) {
+      const uint32_t rs = lane_addr + C::R_COL + (ii & 1) * 128;
+      if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) break;
+      tc_fence_after();
+      const int qs = ii % C::NSQ;
+#pragma unroll
+      for (int c0 = 0; c0 < C::NCHT; c0 += 2) {
+        uint32_t a[2][32];
+        tmem_ld32(rs + 32 * c0, a[0]);
+        tmem_ld32(rs + 32 * (c0 + 1), a[1]);
+        tmem_wait_ld();
+        reg_fence(a[0]);
+        reg_fence(a[1]);
+        stage_chunk(a[0], sb + C::dq_slot(qs, c0, wq));
+        stage_chunk(a[1], sb + C::dq_slot(qs, c0 + 1, wq));
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQDRAINED));
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_STAGED + qs));
+    }
+  } else {
+    // ---------------------------------------------------------------- P, dS
+    // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ; thread r of a
+    // warpgroup owns TMEM lane r (key row r).  The row statistics of query
+    // tile i+1 are loaded from global memory during tile i and published,
+    // through a double-buffered shared array and an mbarrier, right after
+    // dS_i, so the wait for them at the start of tile i+1 rarely blocks.
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;          // key row of Sᵀ / dPᵀ
+    const int kv_row = kv0 + r;
+    const bool row_dead = kv_row >= sp.seqlen;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float c = p.scale_log2;
+    // log2e·LSE (warpgroup 0; +inf past the sequence end, so P = 0 there) or
+    // D (warpgroup 1) of query row r of tile ii.
+    auto load_stat = [&](int ii) -> float {
+      const int q = (i_first + ii) * kTile + r;
+      if (q >= sp.seqlen) return g == 0 ? CUDART_INF_F : 0.f;
+      return g == 0 ? __ldg(p.lse + stat_base + q) * kLog2e : __ldg(p.dpsum + stat_base + q);
+    };
+    // Both warpgroups read all 128 entries of a tile: publish them through an
+    // mbarrier (a bounded wait, unlike a named barrier, so an abort cannot
+    // hang).  Buffer ii & 1 was last read during tile ii - 2, which every
+    // thread has finished once it has passed tile ii - 1's wait.
+    auto publish_stat = [&](int ii, float v) {
+      float* buf = stat + (ii & 1) * 256;
+      buf[g * 128 + r] = v;
+      mbar_arrive(bar(C::B_STAT + (ii & 1)));
+    };
+    if (nq > 0) publish_stat(0, load_stat(0));
+    float stat_next = nq > 1 ? load_stat(1) : 0.f;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int qi = i_first + ii;
       const int q0 = qi * kTile;
       const uint32_t rs = lane_addr + C::R_COL + (ii & 1) * 128;
       const uint32_t rp = lane_addr + C::R_COL + ((ii + 1) & 1) * 128;
-      float* lse2 = stat + (ii & 1) * 256;
-      float* dsum = lse2 + 128;
-      if (g == 0) lse2[r] = stat_next; else dsum[r] = stat_next;
-      if (ii + 1 < nq) stat_next = load_stat(ii + 1);
-      // Both warpgroups read all 128 entries: publish them through an mbarrier
-      // (a bounded wait, unlike a named barrier, so an abort cannot hang here).
-      mbar_arrive(bar(C::B_STAT + (ii & 1)));
+      const float* lse2 = stat + (ii & 1) * 256;
+      const float* dsum = lse2 + 128;
       if (!wait_bounded(bar(C::B_STAT + (ii & 1)), (ii >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
         ok = false;
         break;
@@ -495,27 +527,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-      // ---- dQ_i (query row r, columns g·d/2 ..): stage it over Q_i / dO_i,
-      // free once every MMA of tile i (the last is dQ_i) has completed.
-      // Rows past the sequence end carry exact zeros (their P, hence dS, is 0).
-      if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) {
-        ok = false;
-        break;
+      if (ii + 1 < nq) {
+        publish_stat(ii + 1, stat_next);
+        if (ii + 2 < nq) stat_next = load_stat(ii + 2);
       }
-      tc_fence_after();
-      uint32_t a[NCH][32];
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(rs + g * (D / 2) + 32 * ch, a[ch]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) reg_fence(a[ch]);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DQDRAINED));
-      const int qs = ii % C::NSQ;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) stage_chunk(a[ch], sb + C::dq_slot(qs, g, wq, ch));
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_STAGED + qs));
     }
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
