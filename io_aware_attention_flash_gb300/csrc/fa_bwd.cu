@@ -162,7 +162,13 @@ struct BwdCfg {
   }
   static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
   static constexpr int NUM_DRAIN = 128;                // warps 10-13: one per TMEM lane quarter
-  static constexpr int NUM_THREADS = NUM_COMPUTE + 64 + NUM_DRAIN;
+  // Warps 14-15 only complete the fourth warpgroup, so that registers can be
+  // moved per warpgroup: 512 threads launch with 128 registers each; the two
+  // compute warpgroups take REG_COMPUTE, the other two give back to REG_OTHER.
+  static constexpr int NUM_THREADS = 512;
+  static constexpr int REG_COMPUTE = 168;
+  static constexpr int REG_OTHER = 88;
+  static_assert(256 * REG_COMPUTE + 256 * REG_OTHER <= 65536, "register split exceeds the launch allocation");
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int DRAIN_WARP0 = 10;
@@ -237,6 +243,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 
   if (warp == C::PRODUCER_WARP) {
     // ---------------------------------------------------------------- TMA
+    setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -301,6 +308,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     }
   } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------------- MMA
+    setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
       constexpr uint32_t idesc_sp = idesc_bf16(128, 128, false, false);   // Sᵀ, dPᵀ
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);      // dV, dK (A from TMEM)
@@ -377,8 +385,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       tc_commit(bar(C::B_DRAIN));
       wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
     }
+  } else if (warp >= C::DRAIN_WARP0 + 4) {
+    setmaxnreg_dec<C::REG_OTHER>();        // warps 14-15: no role
   } else if (warp >= C::DRAIN_WARP0) {
     // ---------------------------------------------------------------- dQ drain
+    setmaxnreg_dec<C::REG_OTHER>();
     // One warp per TMEM lane quarter wq (dQ rows 32·wq .. +31 of the query
     // tile; thread = row).  Once dQ_i has completed, copy the rows from TMEM
     // into the 128-byte swizzled staging slices over Q_i / dO_i, two 32-column
@@ -419,6 +430,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- P, dS
+    setmaxnreg_inc<C::REG_COMPUTE>();
     // Warpgroup g owns query columns 64g .. 64g+63 of Sᵀ / dPᵀ; thread r of a
     // warpgroup owns TMEM lane r (key row r).  The row statistics of query
     // tile i+1 are loaded from global memory during tile i and published,
