@@ -184,10 +184,11 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   FA_TRY(bind_device(q));
   uint32_t* err = nullptr;
   FA_TRY(error_word(&err));
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   FA_TRY(make_map(&tq, q, d, H, rows_per_outer, outer));
   FA_TRY(make_map(&tk, k, d, H, rows_per_outer, outer));
   FA_TRY(make_map(&tv, v, d, H, rows_per_outer, outer));
+  FA_TRY(make_map(&to, o, d, H, rows_per_outer, outer));
   fa::FwdParams p{};
   p.sv.cu_seqlens = cu;
   p.sv.H = H;
@@ -199,7 +200,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   p.causal = causal ? 1 : 0;
   p.err = err;
   p.timeout_ns = kWaitLimitNs;
-  const cudaError_t e = fa::launch_fwd(d, tq, tk, tv, p, nseq, max_seqlen, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = fa::launch_fwd(d, tq, tk, tv, to, p, nseq, max_seqlen, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
 }
 

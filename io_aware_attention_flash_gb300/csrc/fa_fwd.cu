@@ -48,7 +48,8 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQT * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
-  // barriers: q, kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT], odone, drain
+  // barriers: q, kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT], odone[NQT],
+  // ostaged[NQT], drain
   static constexpr int B_Q = 0;
   static constexpr int B_KFULL = 1;
   static constexpr int B_KEMPTY = B_KFULL + NSK;
@@ -57,7 +58,8 @@ struct FwdCfg {
   static constexpr int B_SFULL = B_VEMPTY + NSV;
   static constexpr int B_PFULL = B_SFULL + NQT;
   static constexpr int B_ODONE = B_PFULL + NQT;
-  static constexpr int B_DRAIN = B_ODONE + 1;
+  static constexpr int B_OSTAGED = B_ODONE + NQT;       // O_t staged in shared memory for its TMA store
+  static constexpr int B_DRAIN = B_OSTAGED + NQT;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -76,7 +78,8 @@ struct FwdCfg {
 template <int D>
 __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int NQT = C::NQT;
   extern __shared__ uint8_t smem_raw[];
@@ -105,6 +108,38 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
     nkv_max = max(nkv_max, nkv[t]);
   }
 
+  // TMA issue of Q and of K/V tile j into its ring slot (producer thread).
+  auto load_q = [&]() {
+    uint32_t qbytes = 0;
+    for (int t = 0; t < NQT; ++t)
+      if (nkv[t] > 0) qbytes += C::TILE_BYTES;
+    mbar_arrive_expect_tx(bar(C::B_Q), qbytes);
+    for (int t = 0; t < NQT; ++t) {
+      if (nkv[t] == 0) continue;
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_4d(sb + C::OFF_Q + t * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_Q), kb * 64, sp.h,
+                    sp.tma_row0 + q0 + t * kTile, sp.tma_b);
+    }
+  };
+  auto load_k = [&](int j) {
+    const int ks = j % C::NSK;
+    mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + kb * C::BLK_BYTES, &tmK, bar(C::B_KFULL + ks), kb * 64,
+                  sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+  };
+  auto load_v = [&](int j) {
+    const int vs = j % C::NSV;
+    mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmV, bar(C::B_VFULL + vs), kb * 64,
+                  sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+  };
+  // K/V tiles whose ring slots start empty: loaded by the producer as soon as
+  // it has initialised the barriers, so the first loads overlap the TMEM
+  // allocation and the CTA-wide barrier.
+  const int preloaded = min(nkv_max, C::NSV);
+
   if (warp == C::PRODUCER_WARP && lane == 0) {
     mbar_init(bar(C::B_Q), 1);
     for (int s = 0; s < C::NSK; ++s) {
@@ -118,12 +153,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
     for (int t = 0; t < NQT; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
       mbar_init(bar(C::B_PFULL + t), 128);
+      mbar_init(bar(C::B_ODONE + t), 1);
+      mbar_init(bar(C::B_OSTAGED + t), 128);
     }
-    mbar_init(bar(C::B_ODONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    load_q();
+    for (int j = 0; j < preloaded; ++j) {
+      load_k(j);
+      load_v(j);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -137,38 +181,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
   if (warp == C::PRODUCER_WARP) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t qbytes = 0;
-      for (int t = 0; t < NQT; ++t)
-        if (nkv[t] > 0) qbytes += C::TILE_BYTES;
-      mbar_arrive_expect_tx(bar(C::B_Q), qbytes);
-      for (int t = 0; t < NQT; ++t) {
-        if (nkv[t] == 0) continue;
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_4d(sb + C::OFF_Q + t * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_Q), kb * 64, sp.h,
-                      sp.tma_row0 + q0 + t * kTile, sp.tma_b);
-      }
-      int k_fills = 0, v_fills = 0;
-      for (int j = 0; j < nkv_max; ++j) {
+      int k_fills = preloaded, v_fills = preloaded;
+      for (int j = preloaded; j < nkv_max; ++j) {
         const int ks = j % C::NSK;
         if (j >= C::NSK && !wait_bounded(bar(C::B_KEMPTY + ks), ((j / C::NSK) - 1) & 1, abort_flag, p.err,
                                          p.timeout_ns))
           break;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_4d(sb + C::OFF_K + ks * C::TILE_BYTES + kb * C::BLK_BYTES, &tmK, bar(C::B_KFULL + ks),
-                      kb * 64, sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+        load_k(j);
         ++k_fills;
         const int vs = j % C::NSV;
         if (j >= C::NSV && !wait_bounded(bar(C::B_VEMPTY + vs), ((j / C::NSV) - 1) & 1, abort_flag, p.err,
                                          p.timeout_ns))
           break;
-        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_4d(sb + C::OFF_V + vs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmV, bar(C::B_VFULL + vs),
-                      kb * 64, sp.h, sp.tma_row0 + j * kTile, sp.tma_b);
+        load_v(j);
         ++v_fills;
       }
       if (*abort_flag) {
@@ -246,7 +271,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
         tc_commit(bar(C::B_VEMPTY + vs));
         if (next) tc_commit(bar(C::B_KEMPTY + ks1));
       }
-      if (ok) tc_commit(bar(C::B_ODONE));
+      // O_t is final.  (Committing each tile's barrier inside the loop, right
+      // after its last PV, measured slower: this thread's instruction stream
+      // is the loop's limiter.)
+      if (ok)
+        for (int t = 0; t < NQT; ++t) tc_commit(bar(C::B_ODONE + t));
       // Every MMA issued so far must finish before TMEM is released.
       tc_commit(bar(C::B_DRAIN));
       wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
@@ -356,34 +385,59 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + t));
       }
-      if (ok) ok = wait_bounded(bar(C::B_ODONE), 0, abort_flag, p.err, p.timeout_ns);
+      if (ok) ok = wait_bounded(bar(C::B_ODONE + t), 0, abort_flag, p.err, p.timeout_ns);
       if (ok) {
+        // O_t / l, as bf16.  A whole tile (every dense tile: the map clips
+        // rows past N; a packed tile that does not run past its sequence) is
+        // staged in the 128-byte swizzled layout over Q_t, which no MMA reads
+        // any more, and written by one TMA store per 64 columns; a packed tile
+        // that ends inside its sequence's last 128 rows is written row by row
+        // (a box would overwrite the next sequence's rows).
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.0f / l : 0.f;
         const bool store = q_row < sp.seqlen;
+        const bool via_tma = !p.sv.cu_seqlens || qt + kTile <= sp.seqlen;
+        const uint32_t stage = sb + C::OFF_Q + t * C::TILE_BYTES;
         uint16_t* orow = p.o + (static_cast<size_t>(sp.row_base + q_row) * p.sv.H + sp.h) * D;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
+#pragma unroll 1
+        for (int ch = 0; ch < D / 16; ++ch) {  // 16 columns (two 16-byte chunks) at a time
+          uint32_t o[16];
+          tmem_ld16(tO + ch * 16, o);
           tmem_wait_ld();
           reg_fence(o);
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+          uint32_t w[8];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
-              dst[v4] = w;
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (via_tma) {
+            const uint32_t rowaddr = stage + (ch / 4) * C::BLK_BYTES + r * 128;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t chunk = ((ch % 4) * 2 + u) ^ (r & 7);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + chunk * 16), "r"(w[4 * u]),
+                           "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                           : "memory");
             }
+          } else if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
         }
         if (store) {
           const float lse = l > 0.f ? (m_ref * c + log2f(l)) * kLn2 : -CUDART_INF_F;
           p.lse[(static_cast<size_t>(sp.bs) * p.sv.H + sp.h) * p.sv.lse_stride + q_row] = lse;
+        }
+        if (via_tma) {
+          fence_proxy_async_smem();
+          mbar_arrive(bar(C::B_OSTAGED + t));
+          if (r == 0 && wait_bounded(bar(C::B_OSTAGED + t), 0, abort_flag, p.err, p.timeout_ns)) {
+#pragma unroll
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_store_4d(&tmO, stage + kb * C::BLK_BYTES, kb * 64, sp.h, sp.tma_row0 + qt, sp.tma_b);
+            bulk_commit_group();
+            bulk_wait_group0();   // the copies are complete before the CTA exits
+          }
         }
       }
     }
@@ -398,8 +452,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
 }
 
 template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                         int nseq, int max_seqlen, cudaStream_t s) {
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                         const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
   using C = FwdCfg<D>;
   static bool configured = false;  // per process; attribute is per function
   if (!configured) {
@@ -408,16 +462,16 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     configured = true;
   }
   dim3 grid(nseq * p.sv.H, (max_seqlen + kTile * C::NQT - 1) / (kTile * C::NQT));
-  fa_fwd_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, nseq, max_seqlen, s);
-  return launch_fwd_d<128>(tq, tk, tv, p, nseq, max_seqlen, s);
+                       const CUtensorMap& to, const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, p, nseq, max_seqlen, s);
+  return launch_fwd_d<128>(tq, tk, tv, to, p, nseq, max_seqlen, s);
 }
 
 }  // namespace fa

@@ -79,7 +79,7 @@ __device__ __forceinline__ SeqPos seq_pos(const SeqView& sv) {
 
 // Grid sizes / launches (defined next to the kernels).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s);
+                       const CUtensorMap& to, const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
                        cudaStream_t s,
