@@ -209,6 +209,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
   const int i_first = p.causal ? j : 0;
   const int nq = nq_total - i_first;
 
+  // TMA issue of query tile ii's Q and dO into ring slot ii % NSQ (producer
+  // thread).
+  auto load_qdo = [&](int ii) {
+    const int qs = ii % C::NSQ;
+    const int qrow = sp.tma_row0 + (i_first + ii) * kTile;
+    mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_Q + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_QFULL + qs), kb * 64, sp.h,
+                  qrow, sp.tma_b);
+    mbar_arrive_expect_tx(bar(C::B_DOFULL + qs), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_DO + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmdO, bar(C::B_DOFULL + qs), kb * 64,
+                  sp.h, qrow, sp.tma_b);
+  };
+  // K, V and the query tiles whose ring slots start empty are loaded by the
+  // producer as soon as it has initialised the barriers, so the first loads
+  // overlap the TMEM allocation and the CTA-wide barrier.
+  const int preloaded = min(nq, C::NSQ);
+
   if (warp == C::PRODUCER_WARP && lane == 0) {
     mbar_init(bar(C::B_KV), 1);
     for (int s = 0; s < C::NSQ; ++s) {
@@ -229,6 +248,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+    mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_4d(sb + C::OFF_K + kb * C::BLK_BYTES, &tmK, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
+                  sp.tma_b);
+      tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
+                  sp.tma_b);
+    }
+    for (int ii = 0; ii < preloaded; ++ii) load_qdo(ii);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -245,17 +276,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     // ---------------------------------------------------------------- TMA
     setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_4d(sb + C::OFF_K + kb * C::BLK_BYTES, &tmK, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
-                    sp.tma_b);
-        tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
-                    sp.tma_b);
-      }
       // The dQ of query tile t is staged (fp32, 128-byte swizzled, one 4 KB
       // slice per 32 rows and 32 columns) over Q_t and dO_t in ring slot
       // t % NSQ once the MMAs have consumed them.  This thread adds
@@ -274,22 +294,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         bulk_commit_group();
         return true;
       };
-      int fills = 0;
-      for (int ii = 0; ii < nq; ++ii) {
-        const int qs = ii % C::NSQ;
-        const int qrow = sp.tma_row0 + (i_first + ii) * kTile;
-        if (ii >= C::NSQ) {
-          if (!reduce_tile(ii - C::NSQ)) break;
-          bulk_wait_group_read0();   // the slot's staged dQ has been read
-        }
-        mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_4d(sb + C::OFF_Q + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_QFULL + qs),
-                      kb * 64, sp.h, qrow, sp.tma_b);
-        mbar_arrive_expect_tx(bar(C::B_DOFULL + qs), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_4d(sb + C::OFF_DO + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmdO, bar(C::B_DOFULL + qs),
-                      kb * 64, sp.h, qrow, sp.tma_b);
+      int fills = preloaded;
+      for (int ii = preloaded; ii < nq; ++ii) {
+        if (!reduce_tile(ii - C::NSQ)) break;
+        bulk_wait_group_read0();   // the slot's staged dQ has been read
+        load_qdo(ii);
         ++fills;
       }
       if (!*abort_flag) {
