@@ -9,7 +9,9 @@ from .attention import (  # noqa: F401
     backward,
     backward_rows,
     backward_varlen,
+    decode_mask,
     forward,
+    forward_decode,
     forward_rows,
     forward_varlen,
     softmax_rows,

@@ -26,6 +26,13 @@ What it computes, and where that is defined:
   is visible to query i iff j <= i; with equal query and key lengths no row is
   ever fully masked.  A fully masked row (not reachable by the configurations
   here) is defined as O = 0, LSE = −inf.
+* Decoding against a key/value cache, "LLM Systems 22" section 5.1: a few
+  new query tokens (Nq, typically 1 to 4) attend to a long cache of Nk keys.
+  Reading taken: the new tokens are the last Nq positions of the sequence, so
+  under a causal mask query i sees keys j <= Nk − Nq + i (with Nq = Nk this
+  is the causal mask above; with Nq = 1 it is every key).  Split-KV
+  (section 5.2) changes only how the GPU divides the work, not the result,
+  so the oracle is the same one-shot definition.
 * Variable-length batches, "08 · FlashAttention" section 四 (packing with
   ``cu_seqlens`` instead of a padding mask): sequences are independent; each
   is the batched definition with B = 1 applied to its own rows.
@@ -55,6 +62,8 @@ __all__ = [
     "backward_rows",
     "forward_varlen",
     "backward_varlen",
+    "decode_mask",
+    "forward_decode",
 ]
 
 # Row panel height used to bound memory at long sequence lengths.  Panels only
@@ -228,3 +237,35 @@ def backward_varlen(q, k, v, do, cu_seqlens, scale: float, causal: bool):
         dq, dk, dv = backward(q[None, s:e], k[None, s:e], v[None, s:e], do[None, s:e], scale, causal)
         dQ[s:e], dK[s:e], dV[s:e] = dq[0], dk[0], dv[0]
     return dQ, dK, dV
+
+
+def decode_mask(n_q: int, n_k: int, causal: bool) -> np.ndarray:
+    """Boolean [n_q, n_k]: cache key j visible to new query token i.
+
+    Causal: j <= n_k − n_q + i (the new tokens are the sequence's last n_q
+    positions); otherwise every key.
+    """
+    if not causal:
+        return np.ones((n_q, n_k), dtype=bool)
+    return np.arange(n_k, dtype=np.int64)[None, :] <= (n_k - n_q + np.arange(n_q, dtype=np.int64))[:, None]
+
+
+def forward_decode(q, k, v, scale: float, causal: bool):
+    """Decode forward: q [B, Nq, H, d] against a cache k, v [B, Nk, H, d].
+
+    Returns O [B, Nq, H, d] and LSE [B, H, Nq] (float64): the three-step
+    definition with the mask of ``decode_mask``.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    mask = decode_mask(Nq, Nk, causal)
+    O = np.zeros((B, Nq, H, d))
+    L = np.zeros((B, H, Nq))
+    for b in range(B):
+        for h in range(H):
+            S = scale * (q[b, :, h, :] @ k[b, :, h, :].T)
+            P, lse = softmax_rows(S, mask)
+            O[b, :, h, :] = P @ v[b, :, h, :]
+            L[b, h, :] = lse
+    return O, L
