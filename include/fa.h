@@ -136,6 +136,26 @@ FA_API fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, cons
                         int causal, void* stream);
 
 /*
+ * Decode forward against a key/value cache, split along the cache ("LLM
+ * Systems 22: Flash Attention", sections 5.1 and 5.2: Split-KV /
+ * Flash-Decoding).  q, o: bf16 [B, Nq, H, d], the Nq (1 .. 8) newest tokens;
+ * k, v: bf16 [B, Nk, H, d], the whole cache including those tokens.  lse:
+ * fp32 [B, H, Nq].  causal != 0: the new tokens are the cache's last Nq
+ * positions, so query i sees keys j <= Nk − Nq + i (lower-right alignment;
+ * with Nq = 1 every key); causal == 0: every key.  The cache is split into
+ * chunks of 128 to 1024 keys; each chunk's partial softmax statistics and
+ * unnormalised output go to `workspace` (at least
+ * fa_decode_workspace_bytes(B, H, Nq, Nk, d) bytes, 16-byte aligned, caller
+ * owned) and a second kernel merges them.  Other conventions as fa_fwd.
+ * Nq outside 1 .. 8 or Nk < 1 is FA_ERR_SHAPE; a short workspace is
+ * FA_ERR_WORKSPACE.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                               size_t workspace_bytes, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                               void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns FA_OK, FA_ERR_TIMEOUT (some kernel's bounded mbarrier wait
  * ran out and the kernel returned early: its outputs are invalid) or

@@ -17,6 +17,8 @@ import torch
 from . import _binding
 from ._binding import (  # noqa: F401  (C-ABI names)
     FaError,
+    fa_decode_workspace_bytes,
+    fa_fwd_decode,
     fa_bwd,
     fa_bwd_varlen,
     fa_bwd_varlen_workspace_bytes,
@@ -32,6 +34,7 @@ __all__ = [
     "attention_forward", "attention_backward", "attention_forward_varlen", "attention_backward_varlen",
     "flash_attention", "FaError", "fa_fwd", "fa_bwd", "fa_fwd_varlen", "fa_bwd_varlen",
     "fa_bwd_workspace_bytes", "fa_bwd_varlen_workspace_bytes", "fa_get_device_error", "load_library",
+    "attention_decode", "fa_fwd_decode", "fa_decode_workspace_bytes",
 ]
 
 
@@ -46,6 +49,22 @@ def attention_forward(q, k, v, causal: bool = False, scale=None, stream=None):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_decode(q, k, v, causal: bool = False, scale=None, stream=None, workspace=None):
+    """Decode: q [B,Nq,H,d] (Nq <= 8 newest tokens) against the cache k, v
+    [B,Nk,H,d].  Returns (o [B,Nq,H,d] bf16, lse [B,H,Nq] fp32).  causal: the
+    new tokens are the cache's last Nq positions (query i sees keys
+    j <= Nk - Nq + i)."""
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(fa_decode_workspace_bytes(B, H, Nq, Nk, d), 16), device=q.device,
+                                dtype=torch.uint8)
+    fa_fwd_decode(q, k, v, o, lse, workspace, causal, scale, stream)
     return o, lse
 
 

@@ -40,6 +40,8 @@ SIGNATURES = {
     "fa_last_error_detail": (ctypes.c_char_p, []),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_microbench": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double), _P]),
+    "fa_decode_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
+    "fa_fwd_decode": (_I, [_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _F, _I, _P]),
 }
 
 # fa_microbench selectors: rate per SM per SM-clock of each unit.
@@ -190,6 +192,24 @@ def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, max_
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(cu_seqlens), nseq, max_seqlen, T, H, d,
         _scale(scale, d), int(bool(causal)), _stream(stream)))
+
+
+def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(lib().fa_decode_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_fwd_decode(q, k, v, o, lse, workspace, causal: bool, scale=None, stream=None) -> None:
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    _bf16("q", q, (B, Nq, H, d))
+    _bf16("o", o, (B, Nq, H, d))
+    for n, t in (("k", k), ("v", v)):
+        _bf16(n, t, (B, Nk, H, d))
+    _f32("lse", lse, (B, H, Nq))
+    _check("fa_fwd_decode", lib().fa_fwd_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), B, H, Nq, Nk, d, _scale(scale, d), int(bool(causal)),
+        _stream(stream)))
 
 
 def fa_get_device_error(stream=None) -> int:

@@ -24,7 +24,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_microbench.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_microbench.cu"]
 HEADERS = ["ptx.cuh", "fa_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

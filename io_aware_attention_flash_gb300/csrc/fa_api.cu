@@ -273,6 +273,34 @@ __global__ void fa_wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns
   __syncthreads();
 }
 
+// Split-KV decode: keys per split and number of splits.  A split is 1 to 8
+// key tiles, sized so that there are about four work items per SM of a
+// GB300 (152 SMs) where the cache allows; the choice depends only on the
+// shapes, so the workspace size does too.
+void decode_split(int B, int H, int Nk, int* splits, int* split_len) {
+  constexpr long long kTargetItems = 4 * 152;
+  const long long tiles = (Nk + fa::kTile - 1) / fa::kTile;
+  long long per = (tiles * B * H + kTargetItems - 1) / kTargetItems;
+  per = per < 1 ? 1 : (per > 8 ? 8 : per);
+  *split_len = static_cast<int>(per * fa::kTile);
+  *splits = static_cast<int>((Nk + *split_len - 1) / *split_len);
+}
+
+size_t decode_ws_bytes(int B, int H, int Nq, int Nk, int d) {
+  int splits = 0, split_len = 0;
+  decode_split(B, H, Nk, &splits, &split_len);
+  const size_t parts = static_cast<size_t>(B) * H * splits * 4 * Nq;
+  return pad256(parts * d * 4) + pad256(parts * 2 * 4);
+}
+
+fa_status check_decode(int B, int H, int Nq, int Nk, int d, float scale) {
+  FA_TRY(check_common(H, d, scale));
+  if (B <= 0 || Nq <= 0 || Nq > 8 || Nk <= 0) return FA_ERR_SHAPE;
+  FA_TRY(check_rows(B, static_cast<long long>(B) * Nk, Nk, H, d));
+  if (static_cast<long long>(B) * H * Nq > (1LL << 31) / 32) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
 }  // namespace
 
 namespace fa {
@@ -348,6 +376,51 @@ FA_API fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, cons
   FA_TRY(check_rows(nseq, total, max_seqlen, H, d));
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, cu_seqlens, nseq, max_seqlen, total,
                   1, H, d, scale, causal, stream);
+}
+
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode(B, H, Nq, Nk, d, 1.0f) != FA_OK) return 0;
+  return decode_ws_bytes(B, H, Nq, Nk, d);
+}
+
+FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                               size_t workspace_bytes, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                               void* stream) {
+  FA_TRY(check_decode(B, H, Nq, Nk, d, scale));
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+    return FA_ERR_ALIGN;
+  if (workspace_bytes < decode_ws_bytes(B, H, Nq, Nk, d)) return FA_ERR_WORKSPACE;
+  FA_TRY(bind_device(q));
+  uint32_t* err = nullptr;
+  FA_TRY(error_word(&err));
+  CUtensorMap tk, tv;
+  FA_TRY(make_map(&tk, k, d, H, Nk, B));
+  FA_TRY(make_map(&tv, v, d, H, Nk, B));
+  fa::DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  decode_split(B, H, Nk, &p.splits, &p.split_len);
+  const size_t parts = static_cast<size_t>(B) * H * p.splits * 4 * Nq;
+  p.o_part = static_cast<float*>(workspace);
+  p.ml_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pad256(parts * d * 4));
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.scale_log2 = scale * fa::kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.err = err;
+  p.timeout_ns = kWaitLimitNs;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail("device query", e);
+  const long long items = static_cast<long long>(B) * H * p.splits;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  e = fa::launch_decode(d, tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("decode launch", e);
 }
 
 FA_API fa_status fa_get_device_error(void* stream) {

@@ -1,0 +1,348 @@
+// Split-KV decode forward for sm_103a ("LLM Systems 22: Flash Attention",
+// sections 5.1 and 5.2): a few new query tokens per head (Nq <= 8) attend to
+// a long key/value cache.  With so few query rows there is one tiny GEMV per
+// head, far too little parallel work along the query dimension, and the cost
+// is reading K and V once: the work is split along the key/value length, each
+// split keeps its own softmax statistics (m, l) and unnormalised output, and a
+// light merge combines them.
+//
+//   fa_decode_split_kernel  persistent (one CTA per SM); CTA c takes work items
+//                           c, c + G, ... where item = (sequence·head, split).
+//                           Warp 4 streams the 128-key K and V tiles of its
+//                           items through a 3-stage TMA ring without draining
+//                           between items; warps 0-3 each own 32 keys of every
+//                           tile and keep their own partial softmax (so the
+//                           four warps never synchronise with each other) and
+//                           write one partial (m, l, O) per item.
+//   fa_decode_merge_kernel  one warp per (sequence, head, query): combines the
+//                           4·S partials into O (bf16) and LSE.
+//
+// The bytes are the cost (K and V once, 4·d bytes per cached token and head),
+// so the arithmetic runs on the FMA pipe: lanes split the head dimension for
+// q·k, and one 31-shuffle transpose-reduction per query leaves each lane the
+// score of one key.  Scores are kept in base-2 units (c = scale·log2 e).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "fa_kernels.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct DecCfg {
+  static constexpr int KB = D / 64;                    // 128-byte swizzle blocks per row
+  static constexpr int BLK_BYTES = kTile * 128;        // 128 rows x 64 bf16
+  static constexpr int TILE_BYTES = KB * BLK_BYTES;    // 128 keys x D
+  static constexpr int NST = 3;                        // ring stages (K and V tile each)
+  static constexpr int NQMAX = 8;
+  static constexpr int E = D / 32;                     // head-dimension elements per lane
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
+  static constexpr int OFF_P = OFF_V + NST * TILE_BYTES;  // [4 warps][NQMAX][32] fp32 probabilities
+  static constexpr int OFF_BAR = OFF_P + 4 * NQMAX * 32 * 4;
+  static constexpr int B_FULL = 0;
+  static constexpr int B_EMPTY = NST;
+  static constexpr int NBAR = 2 * NST;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // abort flag
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
+  static constexpr int NUM_THREADS = 160;              // warps 0-3 compute, warp 4 TMA
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Byte offset, inside a 128-byte swizzled tile, of row j's head-dimension
+// elements E·lane .. E·lane + E - 1 (contiguous: 8 bytes for d = 128, 4 for 64).
+template <int D>
+__device__ __forceinline__ uint32_t row_slice(int j, int lane) {
+  constexpr int E = D / 32;
+  const int c0 = E * lane;                  // first column
+  const int blk = c0 / 64;                  // 64-column block
+  const int byte = (c0 % 64) * 2;           // byte inside the 128-byte row of the block
+  return blk * (kTile * 128) + j * 128 + ((((byte >> 4) ^ (j & 7)) << 4) | (byte & 15));
+}
+
+template <int D>
+__device__ __forceinline__ void load_row_slice(uint32_t addr, float (&x)[D / 32]) {
+  if constexpr (D == 128) {
+    uint32_t a, b;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+    x[0] = bf16lo_to_f32(a);
+    x[1] = bf16hi_to_f32(a);
+    x[2] = bf16lo_to_f32(b);
+    x[3] = bf16hi_to_f32(b);
+  } else {
+    uint32_t a;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a) : "r"(addr));
+    x[0] = bf16lo_to_f32(a);
+    x[1] = bf16hi_to_f32(a);
+  }
+}
+
+// v[i] holds this lane's contribution to element i (32 elements); afterwards
+// v[0] holds the sum over all 32 lanes of element `lane`.
+__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
+    fa_decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const DecodeParams p) {
+  using C = DecCfg<D>;
+  constexpr int E = C::E;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_base + pad;
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = p.B * p.H * p.splits;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::B_FULL + s), 1);
+      mbar_init(bar(C::B_EMPTY + s), 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int t = 0;  // tiles issued by this CTA
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int bh = item / p.splits, split = item - (item / p.splits) * p.splits;
+        const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+        const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
+        for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
+          const int st = t % C::NST;
+          if (t >= C::NST && !wait_bounded(bar(C::B_EMPTY + st), ((t / C::NST) - 1) & 1, abort_flag, p.err,
+                                           p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_4d(sb + C::OFF_K + st * C::TILE_BYTES + kb * C::BLK_BYTES, &tmK, bar(C::B_FULL + st),
+                        kb * 64, h, kt, b);
+            tma_load_4d(sb + C::OFF_V + st * C::TILE_BYTES + kb * C::BLK_BYTES, &tmV, bar(C::B_FULL + st),
+                        kb * 64, h, kt, b);
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy already issued land before the CTA exits.
+        for (int s = 0; s < C::NST && s < t; ++s) {
+          const int last = s + ((t - 1 - s) / C::NST) * C::NST;  // last tile issued into stage s
+          wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- scores, softmax, P·V
+    const float c = p.scale_log2;
+    float* pbuf = reinterpret_cast<float*>(smem + C::OFF_P) + warp * C::NQMAX * 32;
+    int t = 0;  // tiles consumed
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const int bh = item / p.splits, split = item - (item / p.splits) * p.splits;
+      const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+      const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
+      float qv[NQ][E], o[NQ][E], m[NQ], lp[NQ];
+#pragma unroll
+      for (int qq = 0; qq < NQ; ++qq) {
+        const int qi = qq < p.Nq ? qq : 0;
+        const uint16_t* qrow = p.q + ((static_cast<size_t>(b) * p.Nq + qi) * p.H + h) * D + E * lane;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          qv[qq][e] = __uint_as_float(static_cast<uint32_t>(qrow[e]) << 16);
+          o[qq][e] = 0.f;
+        }
+        m[qq] = -CUDART_INF_F;
+        lp[qq] = 0.f;
+      }
+      for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
+        const int st = t % C::NST;
+        if (!wait_bounded(bar(C::B_FULL + st), (t / C::NST) & 1, abort_flag, p.err, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ktile = sb + C::OFF_K + st * C::TILE_BYTES;
+        const uint32_t vtile = sb + C::OFF_V + st * C::TILE_BYTES;
+        const int key = kt + warp * 32 + lane;  // this lane's key after the reduction
+        // ---- scores of this warp's 32 keys, one query at a time (not unrolled:
+        // one set of 32 partial dot products live at a time)
+        float sc[NQ];
+#pragma unroll 1
+        for (int qq = 0; qq < NQ; ++qq) {
+          float qcur[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) qcur[e] = qv[qq][e];
+          float part[32];
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk) {
+            float kx[E];
+            load_row_slice<D>(ktile + row_slice<D>(warp * 32 + kk, lane), kx);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc = fmaf(qcur[e], kx[e], acc);
+            part[kk] = acc;
+          }
+          transpose_reduce32(part, lane);
+          // Causal: the new tokens are the last Nq positions, so query qq sees
+          // keys up to Nk - Nq + qq.
+          const int lim = p.causal ? p.Nk - p.Nq + qq : p.Nk - 1;
+          sc[qq] = (qq < p.Nq && key <= lim && key < p.Nk) ? part[0] * c : -CUDART_INF_F;
+        }
+        // ---- online softmax over the warp's keys, per query
+#pragma unroll
+        for (int qq = 0; qq < NQ; ++qq) {
+          float mt = sc[qq];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+          const float m_new = fmaxf(m[qq], mt);
+          const float alpha = (m[qq] == -CUDART_INF_F) ? 0.f : ex2_approx(m[qq] - m_new);
+          const float pr = (sc[qq] == -CUDART_INF_F) ? 0.f : ex2_approx(sc[qq] - m_new);
+          lp[qq] = lp[qq] * alpha + pr;
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[qq][e] *= alpha;
+          m[qq] = m_new;
+          pbuf[qq * 32 + lane] = pr;
+        }
+        __syncwarp();
+        // ---- O += P V over the warp's 32 keys (lane = head-dimension slice)
+#pragma unroll 4
+        for (int kk = 0; kk < 32; ++kk) {
+          float vx[E];
+          load_row_slice<D>(vtile + row_slice<D>(warp * 32 + kk, lane), vx);
+#pragma unroll
+          for (int qq = 0; qq < NQ; ++qq) {
+            const float pq = pbuf[qq * 32 + kk];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[qq][e] = fmaf(pq, vx[e], o[qq][e]);
+          }
+        }
+        __syncwarp();
+        mbar_arrive(bar(C::B_EMPTY + st));
+      }
+      if (!ok) break;
+      // ---- this warp's partial for the item: (m, l, unnormalised O) per query
+      const size_t part_idx = static_cast<size_t>(item) * 4 + warp;
+#pragma unroll
+      for (int qq = 0; qq < NQ; ++qq) {
+        if (qq >= p.Nq) break;
+        float l = lp[qq];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        float* op = p.o_part + (part_idx * p.Nq + qq) * D + E * lane;
+#pragma unroll
+        for (int e = 0; e < E; ++e) op[e] = o[qq][e];
+        if (lane == 0) {
+          p.ml_part[(part_idx * p.Nq + qq) * 2 + 0] = m[qq];
+          p.ml_part[(part_idx * p.Nq + qq) * 2 + 1] = l;
+        }
+      }
+    }
+  }
+}
+
+// One warp per (sequence, head, query): O = Σ 2^(m_p − m) O_p / Σ 2^(m_p − m) l_p
+// over the 4·splits partials of the head, m = max m_p; LSE = ln 2 · (m + log2 l).
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams p) {
+  constexpr int E = D / 32;
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.B * p.H * p.Nq) return;
+  const int qq = wid % p.Nq, bh = wid / p.Nq;
+  const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+  const int n_part = 4 * p.splits;
+  const size_t part0 = static_cast<size_t>(bh) * n_part;
+  float mmax = -CUDART_INF_F;
+  for (int i = lane; i < n_part; i += 32) mmax = fmaxf(mmax, p.ml_part[((part0 + i) * p.Nq + qq) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, off));
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  if (mmax != -CUDART_INF_F) {
+    for (int i = 0; i < n_part; ++i) {
+      const size_t idx = (part0 + i) * p.Nq + qq;
+      const float mp = p.ml_part[idx * 2];
+      if (mp == -CUDART_INF_F) continue;
+      const float w = ex2_approx(mp - mmax);
+      l = fmaf(w, p.ml_part[idx * 2 + 1], l);
+      const float* op = p.o_part + idx * D + E * lane;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, op[e], acc[e]);
+    }
+  }
+  const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+  uint16_t* orow = p.o + ((static_cast<size_t>(b) * p.Nq + qq) * p.H + h) * D + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(acc[e] * inv_l, acc[e + 1] * inv_l);
+  if (lane == 0)
+    p.lse[(static_cast<size_t>(b) * p.H + h) * p.Nq + qq] = l > 0.f ? (mmax + log2f(l)) * kLn2 : -CUDART_INF_F;
+}
+
+template <int D, int NQ>
+cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                             cudaStream_t s) {
+  using C = DecCfg<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_split_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fa_decode_split_kernel<D, NQ><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
+  fa_decode_merge_kernel<D><<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                            cudaStream_t s) {
+  if (p.Nq <= 1) return launch_decode_dq<D, 1>(tk, tv, p, grid, s);
+  if (p.Nq <= 2) return launch_decode_dq<D, 2>(tk, tv, p, grid, s);
+  if (p.Nq <= 4) return launch_decode_dq<D, 4>(tk, tv, p, grid, s);
+  return launch_decode_dq<D, 8>(tk, tv, p, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                          cudaStream_t s) {
+  if (d == 64) return launch_decode_d<64>(tk, tv, p, grid, s);
+  return launch_decode_d<128>(tk, tv, p, grid, s);
+}
+
+}  // namespace fa

@@ -52,6 +52,22 @@ struct BwdParams {
   uint64_t timeout_ns;
 };
 
+// Split-KV decode (fa_decode.cu): q [B, Nq, H, d] against k, v [B, Nk, H, d].
+struct DecodeParams {
+  const uint16_t* q;      // bf16 [B, Nq, H, d]
+  uint16_t* o;            // bf16 [B, Nq, H, d]
+  float* lse;             // fp32 [B, H, Nq]
+  float* o_part;          // fp32 [B·H·splits·4, Nq, d]: unnormalised partial outputs
+  float* ml_part;         // fp32 [B·H·splits·4, Nq, 2]: (max, sum) of each partial, base 2
+  int B, H, Nq, Nk;
+  int splits;             // key/value splits per (sequence, head)
+  int split_len;          // keys per split, a multiple of 128
+  float scale_log2;
+  int causal;             // new tokens are the last Nq positions (lower-right alignment)
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
 // Position of a CTA's (sequence, head): blockIdx.x = sequence * H + head.
 struct SeqPos {
   int bs, h, seq_start, seqlen, row_base, tma_row0, tma_b;
@@ -84,6 +100,8 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
                        cudaStream_t s,
                        cudaEvent_t main_start = nullptr, cudaEvent_t main_end = nullptr);
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                          cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s);
 cudaError_t run_reduce_microbench(int which, int iters, const CUtensorMap& tm, float* buf, int rows, double* result,

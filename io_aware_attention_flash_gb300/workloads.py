@@ -19,7 +19,8 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "make_inputs", "make_varlen_inputs", "flops_fwd", "flops_bwd",
-           "min_hbm_bytes_fwd", "min_hbm_bytes_bwd", "cu_seqlens_from_lengths"]
+           "min_hbm_bytes_fwd", "min_hbm_bytes_bwd", "cu_seqlens_from_lengths", "DecodeWorkload",
+           "DECODE_WORKLOADS", "make_decode_inputs", "min_hbm_bytes_decode"]
 
 
 @dataclass(frozen=True)
@@ -56,6 +57,32 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new tokens per (sequence, head) against a cache of Nk keys/values."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    amplitude: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Decode ("LLM Systems 22", section 5.1: one to a few new tokens against a long
+# cache): 4 sequences x 32 heads, a 32768-token cache (2 GiB of K and V, far
+# beyond L2), one new token, and four (a short speculative / multi-token step).
+DECODE_WORKLOADS = {
+    "decode_n32768": DecodeWorkload("decode_n32768", B=4, H=32, Nq=1, Nk=32768, d=128, causal=True),
+    "decode4_n32768": DecodeWorkload("decode4_n32768", B=4, H=32, Nq=4, Nk=32768, d=128, causal=True),
+}
+
+
 def _draw(gen: torch.Generator, shape, amplitude: float) -> torch.Tensor:
     x = torch.randn(*shape, generator=gen, dtype=torch.float32)
     if amplitude != 1.0:
@@ -67,6 +94,16 @@ def make_inputs(B: int, N: int, H: int, d: int, seed: int = 0, amplitude: float 
     """Q, K, V, dO as CPU bf16 tensors of shape [B, N, H, d]."""
     gen = torch.Generator().manual_seed(seed)
     return tuple(_draw(gen, (B, N, H, d), amplitude) for _ in range(4))
+
+
+def make_decode_inputs(B: int, Nq: int, Nk: int, H: int, d: int, seed: int = 0, amplitude: float = 1.0):
+    """Q [B, Nq, H, d] and K, V [B, Nk, H, d] as CPU bf16 tensors, drawn in
+    that order from one generator seeded with ``seed``."""
+    gen = torch.Generator().manual_seed(seed)
+    q = _draw(gen, (B, Nq, H, d), amplitude)
+    k = _draw(gen, (B, Nk, H, d), amplitude)
+    v = _draw(gen, (B, Nk, H, d), amplitude)
+    return q, k, v
 
 
 def cu_seqlens_from_lengths(lengths) -> torch.Tensor:
@@ -122,3 +159,8 @@ def min_hbm_bytes_fwd(H: int, d: int, total_rows: int) -> float:
 def min_hbm_bytes_bwd(H: int, d: int, total_rows: int) -> float:
     """Q, K, V, O, dO read and dQ, dK, dV written (bf16), plus LSE in and D."""
     return 8.0 * 2.0 * H * d * total_rows + 2.0 * 4.0 * H * total_rows
+
+
+def min_hbm_bytes_decode(B: int, H: int, Nq: int, Nk: int, d: int) -> float:
+    """K and V read once, Q read and O written (bf16), plus the fp32 LSE."""
+    return 2.0 * 2.0 * B * Nk * H * d + 2.0 * 2.0 * B * Nq * H * d + 4.0 * B * H * Nq

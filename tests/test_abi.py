@@ -113,3 +113,27 @@ def test_noalloc_limit_matches_header_and_rejects_on_host(lib):
     # 33.8 MB of workspace needed: rejected before any CUDA call
     assert lib.fa_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                               1, 16, 4096, 128, 0.1, 1, None) == 11
+
+
+def test_decode_validation(lib):
+    ws = lib.fa_decode_workspace_bytes(2, 4, 3, 1000, 128)
+    assert ws > 0 and ws % 256 == 0
+    assert lib.fa_decode_workspace_bytes(2, 4, 0, 1000, 128) == 0
+    assert lib.fa_decode_workspace_bytes(2, 4, 9, 1000, 128) == 0
+    assert lib.fa_decode_workspace_bytes(2, 4, 3, 0, 128) == 0
+    assert lib.fa_decode_workspace_bytes(2, 4, 3, 1000, 96) == 0
+    # one query per partial more costs more workspace; a longer cache never less
+    assert lib.fa_decode_workspace_bytes(2, 4, 4, 1000, 128) > ws
+    assert lib.fa_decode_workspace_bytes(2, 4, 3, 5000, 128) >= ws
+
+    def dec(Nq=3, Nk=1000, d=128, ws_ptr=FAKE, ws_bytes=ws, q=FAKE):
+        return lib.fa_fwd_decode(q, FAKE, FAKE, FAKE, FAKE, ws_ptr, ws_bytes, 2, 4, Nq, Nk, d, 0.1, 1, None)
+
+    assert dec(Nq=0) == 4
+    assert dec(Nq=9) == 4
+    assert dec(Nk=0) == 4
+    assert dec(d=96) == 3
+    assert dec(q=NUL) == 1
+    assert dec(ws_ptr=NUL) == 1
+    assert dec(ws_ptr=FAKE + 8) == 2
+    assert dec(ws_bytes=ws - 1) == 8
