@@ -293,6 +293,8 @@ def run_gpu(args, w):
         "gpu_launches": 4 * K,
         "clocks": clocks.summary(),
     }
+    if not args.no_decode:
+        result["decode"] = run_decode(fa, dev, flush, 20, args.warmup, args.seed + rank, hbm_peak)
     if e2e is not None:
         result["e2e"] = {"value": whole_job_tflops(ws_n, f_fwd + f_bwd, e2e["ms"]), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"]}
@@ -308,6 +310,47 @@ def run_gpu(args, w):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def run_decode(fa, dev, flush, steps: int, warmup: int, seed: int, hbm_peak: float):
+    """Split-KV decode ("LLM Systems 22", section 5.2) on the decode workloads:
+    K and V read once is the whole cost, so the roofline is HBM bandwidth.
+    Each call (split + merge kernels) is timed with CUDA events on the
+    launching stream, L2 flushed between calls (the 2 GiB cache exceeds L2
+    anyway)."""
+    out = []
+    stream = torch.cuda.current_stream(dev)
+    for name in sorted(wl.DECODE_WORKLOADS):
+        w = wl.DECODE_WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in wl.make_decode_inputs(w.B, w.Nq, w.Nk, w.H, w.d, seed, w.amplitude))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Nq), device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d), device=dev, dtype=torch.uint8)
+        for _ in range(max(3, warmup)):
+            fa.fa_fwd_decode(q, k, v, o, lse, ws, w.causal)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fa.fa_fwd_decode(q, k, v, o, lse, ws, w.causal)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if fa.fa_get_device_error() != 0:
+            raise RuntimeError("device error during the decode timing")
+        ms = max_over_ranks([statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)], dev)[0]
+        nbytes = wl.min_hbm_bytes_decode(w.B, w.H, w.Nq, w.Nk, w.d)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out.append({"workload": f"{name}: B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} d={w.d} "
+                                f"{'causal (lower-right)' if w.causal else 'non-causal'}",
+                    "ms": ms, "gpu_launches": 2 * steps,
+                    "roofline": {"kernels": "fa_decode_split_kernel + fa_decode_merge_kernel", "bound": "hbm",
+                                 "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                                 "algorithmic_bytes": nbytes,
+                                 "peak_source": "measured copy (MEASURED_PEAKS.json)"}})
+        del q, k, v, o, lse, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def max_over_ranks(values, device):
@@ -395,6 +438,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
