@@ -209,6 +209,11 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *          15: case 14 with the array read as 128-row tiles, so that one
  *              warp instruction adds 512 contiguous bytes
  *          16: cases 12 and 15 at once, from half the warps each
+ *          17: case 8 while two more warps on the issuing warp's SM
+ *              sub-partition run a softmax-like FMA / ex2 loop
+ *          18, 19, 20: case 8 with the issuing thread idle for 256, 600
+ *              or 1200 cycles once per iteration (32 MMAs, 2048 cycles of
+ *              tensor work): how much queued work covers a pause in issue
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

@@ -54,7 +54,9 @@ MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk"
               "fwd_mma_stream_flop_per_sm_clk_d128_pv_first": 11,
               "tma_reduce_bytes_per_sm_clk": 12, "tma_reduce_bytes_per_sm_clk_2slots": 13,
               "red_v4_bytes_per_sm_clk": 14, "red_v4_coalesced_bytes_per_sm_clk": 15,
-              "tma_and_red_v4_bytes_per_sm_clk": 16}
+              "tma_and_red_v4_bytes_per_sm_clk": 16, "fwd_mma_stream_flop_per_sm_clk_d128_busy": 17,
+              "fwd_mma_stream_flop_per_sm_clk_d128_gap256": 18, "fwd_mma_stream_flop_per_sm_clk_d128_gap600": 19,
+              "fwd_mma_stream_flop_per_sm_clk_d128_gap1200": 20}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

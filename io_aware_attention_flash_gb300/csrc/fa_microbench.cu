@@ -146,18 +146,24 @@ cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_
 // (so each S_t overwrites what the preceding PV_t read), otherwise in
 // columns 384 + 64t that no MMA writes.  SPLIT issues both PVs before both
 // S's.  The rate says how fast the tensor pipe retires this stream when no
-// other unit holds it up.
-template <int DPV, bool ALIAS, bool SPLIT>
-__global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
+// other unit holds it up.  With BUSY, two more warps on the issuing warp's
+// SM sub-partition run an FMA / ex2 mix (as softmax warps do) until the MMA
+// loop ends, so the rate shows what sharing the sub-partition's issue slots
+// costs the issuing thread.  The operand descriptors are formed as in the
+// forward kernel (tile bases once, a 64-bit add per K step).
+template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0>
+__global__ void __launch_bounds__(384, 1) fwd_stream_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
   static_assert(ALIAS || DPV == 64, "separate P columns fit only beside 64-column O tiles");
   constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile: two 128-byte swizzled 64-column blocks
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t done_bar;
   __shared__ uint32_t tmem_slot;
+  __shared__ volatile int mma_done;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gen = smem_raw + (base - raw);
   const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) mma_done = 0;
   for (int i = threadIdx.x; i < 3 * TILE / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(gen)[i] =
         make_uint4(random_bf16x2(4 * i), random_bf16x2(4 * i + 1), random_bf16x2(4 * i + 2), random_bf16x2(4 * i + 3));
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  {  // pseudo-random bf16 in every column an MMA may read as P before it is written
+  if (warp < 4) {  // pseudo-random bf16 in every column an MMA may read as P before it is written
     uint32_t z[32];
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     for (int c = 0; c < 512; c += 32) {
@@ -194,17 +200,17 @@ __global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned 
     auto s_col = [](int t) -> uint32_t { return 128u * t; };
     auto o_col = [](int t) -> uint32_t { return 256u + DPV * t; };
     auto p_col = [](int t) -> uint32_t { return ALIAS ? 128u * t : 384u + 64u * t; };
+    const uint64_t dV = sdesc_sw128(sV, 128 * 128, 1024), dQ = sdesc_sw128(sQ, 16, 1024), dK = sdesc_sw128(sK, 16, 1024);
     auto pv = [&](int t) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + o_col(t), tmem + p_col(t) + kk * 8, sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idesc_o, 1u);
+        mma_ts(tmem + o_col(t), tmem + p_col(t) + kk * 8, sdesc_add(dV, kk * 2048), idesc_o, 1u);
     };
     auto sg = [&](int t) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t koff = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-        mma_ss(tmem + s_col(t), sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024), idesc_s,
-               kk > 0 ? 1u : 0u);
+        mma_ss(tmem + s_col(t), sdesc_add(dQ, koff), sdesc_add(dK, koff), idesc_s, kk > 0 ? 1u : 0u);
       }
     };
     const unsigned long long t0 = clock64();
@@ -214,11 +220,31 @@ __global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned 
       } else {
         pv(0); sg(0); pv(1); sg(1);
       }
+      if (GAP > 0) {  // the issuing thread idles GAP cycles once per iteration
+        const long long tg = clock64();
+        while (clock64() - tg < GAP) {
+        }
+      }
     }
     tc_commit(smem_u32(&done_bar));
     wait_drain(smem_u32(&done_bar), 0, err, 2000000000ull);
     const unsigned long long t1 = clock64();
     cycles[blockIdx.x] = t1 - t0;
+    mma_done = 1;
+  } else if (BUSY && (warp == 4 || warp == 8)) {
+    // Softmax-like issue load on sub-partition 0: FMA, ex2 and add per element,
+    // until the MMA loop is done (and at most 2^22 rounds).
+    float x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = -1.0f - 0.001f * (threadIdx.x + c);
+    for (int it = 0; it < (1 << 22) && !mma_done; ++it) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[c] = ex2_approx(fmaf(x[c], 0.999f, -0.001f)) - 1.5f;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc += x[c];
+    if (acc == 12345.f) cycles[blockIdx.x] = 0;  // keeps the loop alive
   }
   tc_fence_before();
   __syncthreads();
@@ -228,13 +254,13 @@ __global__ void __launch_bounds__(128, 1) fwd_stream_kernel(int iters, unsigned 
   }
 }
 
-template <int DPV, bool ALIAS, bool SPLIT>
+template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0>
 cudaError_t launch_fwd_stream(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
   const int smem = 3 * 128 * 128 * 2 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<DPV, ALIAS, SPLIT>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<DPV, ALIAS, SPLIT, BUSY, GAP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_stream_kernel<DPV, ALIAS, SPLIT><<<sms, 128, smem, s>>>(iters, cyc, err);
+  fwd_stream_kernel<DPV, ALIAS, SPLIT, BUSY, GAP><<<sms, BUSY ? 384 : 128, smem, s>>>(iters, cyc, err);
   return cudaGetLastError();
 }
 
@@ -357,6 +383,10 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 9: e = launch_fwd_stream<64, true, false>(sms, iters, cyc, err, s); break;
     case 10: e = launch_fwd_stream<64, false, false>(sms, iters, cyc, err, s); break;
     case 11: e = launch_fwd_stream<128, true, true>(sms, iters, cyc, err, s); break;
+    case 17: e = launch_fwd_stream<128, true, false, true>(sms, iters, cyc, err, s); break;
+    case 18: e = launch_fwd_stream<128, true, false, false, 256>(sms, iters, cyc, err, s); break;
+    case 19: e = launch_fwd_stream<128, true, false, false, 600>(sms, iters, cyc, err, s); break;
+    case 20: e = launch_fwd_stream<128, true, false, false, 1200>(sms, iters, cyc, err, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;

@@ -21,6 +21,10 @@ pytestmark = gpu
     ("fwd_mma_stream_flop_per_sm_clk_pv64", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_pv64_separate_p", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_d128_pv_first", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_busy", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_gap256", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_gap600", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_gap1200", 1024, 32768),
     ("tma_reduce_bytes_per_sm_clk", 0.5, 256),
     ("tma_reduce_bytes_per_sm_clk_2slots", 0.5, 256),
     ("red_v4_bytes_per_sm_clk", 0.5, 256),
