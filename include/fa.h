@@ -214,6 +214,19 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *          18, 19, 20: case 8 with the issuing thread idle for 256, 600
  *              or 1200 cycles once per iteration (32 MMAs, 2048 cycles of
  *              tensor work): how much queued work covers a pause in issue
+ *          21, 22: case 8 with a tcgen05.commit after each S (21) or after
+ *              each PV and each S (22), to an mbarrier nobody waits on
+ *          23: case 22 plus the forward kernel's four mbarrier waits per
+ *              iteration, on an mbarrier whose phase is already complete
+ *          24: case 23 with K and V taken from 3- and 2-slot rings
+ *          25..30: SM cycles one thread spends on a synchronisation step
+ *              (timed around the step and a branch on its result): 25
+ *              mbarrier.try_wait on a completed phase, 26 the same plus
+ *              tcgen05.fence::after_thread_sync, 27 mbarrier.test_wait, 28 a
+ *              volatile shared-memory flag load, 29 tcgen05.commit, 30 the
+ *              timer alone
+ *          31..37: 25..29, the fence alone, and the timer alone, each right
+ *              after the thread issued 16 MMAs (tensor queue full)
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

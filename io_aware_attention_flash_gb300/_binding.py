@@ -56,7 +56,15 @@ MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk"
               "red_v4_bytes_per_sm_clk": 14, "red_v4_coalesced_bytes_per_sm_clk": 15,
               "tma_and_red_v4_bytes_per_sm_clk": 16, "fwd_mma_stream_flop_per_sm_clk_d128_busy": 17,
               "fwd_mma_stream_flop_per_sm_clk_d128_gap256": 18, "fwd_mma_stream_flop_per_sm_clk_d128_gap600": 19,
-              "fwd_mma_stream_flop_per_sm_clk_d128_gap1200": 20}
+              "fwd_mma_stream_flop_per_sm_clk_d128_gap1200": 20,
+              "fwd_mma_stream_flop_per_sm_clk_d128_commit2": 21, "fwd_mma_stream_flop_per_sm_clk_d128_commit4": 22,
+              "fwd_mma_stream_flop_per_sm_clk_d128_waits": 23, "fwd_mma_stream_flop_per_sm_clk_d128_waits_ring": 24,
+              "sync_cycles_try_wait": 25, "sync_cycles_try_wait_fence": 26, "sync_cycles_test_wait": 27,
+              "sync_cycles_flag_load": 28, "sync_cycles_commit": 29, "sync_cycles_timer": 30,
+              "sync_cycles_try_wait_queue_full": 31, "sync_cycles_try_wait_fence_queue_full": 32,
+              "sync_cycles_test_wait_queue_full": 33, "sync_cycles_flag_load_queue_full": 34,
+              "sync_cycles_commit_queue_full": 35, "sync_cycles_fence_queue_full": 36,
+              "sync_cycles_timer_queue_full": 37}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -150,13 +150,22 @@ cudaError_t launch_mma_rate(int sms, int iters, unsigned long long* cyc, uint32_
 // SM sub-partition run an FMA / ex2 mix (as softmax warps do) until the MMA
 // loop ends, so the rate shows what sharing the sub-partition's issue slots
 // costs the issuing thread.  The operand descriptors are formed as in the
-// forward kernel (tile bases once, a 64-bit add per K step).
-template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0>
+// forward kernel (tile bases once, a 64-bit add per K step).  COMMITS = 2
+// adds a tcgen05.commit (to an mbarrier nobody waits on) after each S_t, as
+// the forward kernel signals each S_t to its softmax; COMMITS = 4 adds one
+// after each PV_t too.  WAITS adds, per iteration, the forward kernel's four
+// mbarrier waits (V, K and P_0 before PV_0, P_1 before PV_1) on an mbarrier
+// whose phase has already completed; RING takes the K and V operands from
+// 3- and 2-slot rings indexed by the iteration, as the forward kernel does.
+template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0, int COMMITS = 0, bool WAITS = false,
+          bool RING = false>
 __global__ void __launch_bounds__(384, 1) fwd_stream_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
   static_assert(ALIAS || DPV == 64, "separate P columns fit only beside 64-column O tiles");
   constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile: two 128-byte swizzled 64-column blocks
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t done_bar;
+  __shared__ __align__(8) uint64_t sink_bar;
+  __shared__ __align__(8) uint64_t ready_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int mma_done;
   const uint32_t raw = smem_u32(smem_raw);
@@ -169,7 +178,10 @@ __global__ void __launch_bounds__(384, 1) fwd_stream_kernel(int iters, unsigned 
         make_uint4(random_bf16x2(4 * i), random_bf16x2(4 * i + 1), random_bf16x2(4 * i + 2), random_bf16x2(4 * i + 3));
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&done_bar), 1);
+    mbar_init(smem_u32(&sink_bar), 1);
+    mbar_init(smem_u32(&ready_bar), 1);
     fence_mbar_init();
+    mbar_arrive(smem_u32(&ready_bar));  // phase 0 complete: every wait below passes
   }
   fence_proxy_async_smem();
   if (warp == 0) {
@@ -201,22 +213,52 @@ __global__ void __launch_bounds__(384, 1) fwd_stream_kernel(int iters, unsigned 
     auto o_col = [](int t) -> uint32_t { return 256u + DPV * t; };
     auto p_col = [](int t) -> uint32_t { return ALIAS ? 128u * t : 384u + 64u * t; };
     const uint64_t dV = sdesc_sw128(sV, 128 * 128, 1024), dQ = sdesc_sw128(sQ, 16, 1024), dK = sdesc_sw128(sK, 16, 1024);
+    uint64_t dVi = dV, dKi = dK;  // this iteration's V and K operands
     auto pv = [&](int t) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + o_col(t), tmem + p_col(t) + kk * 8, sdesc_add(dV, kk * 2048), idesc_o, 1u);
+        mma_ts(tmem + o_col(t), tmem + p_col(t) + kk * 8, sdesc_add(dVi, kk * 2048), idesc_o, 1u);
     };
     auto sg = [&](int t) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t koff = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-        mma_ss(tmem + s_col(t), sdesc_add(dQ, koff), sdesc_add(dK, koff), idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + s_col(t), sdesc_add(dQ, koff), sdesc_add(dKi, koff), idesc_s, kk > 0 ? 1u : 0u);
       }
     };
+    const uint32_t ready = smem_u32(&ready_bar);
+    auto wait_ready = [&]() {
+      if (WAITS) {
+        wait_bounded(ready, 0, &mma_done, err, 1000000000ull);
+        tc_fence_after();
+      }
+    };
+    const uint64_t dK_ring0 = dQ, dV_ring0 = sdesc_sw128(sK, 128 * 128, 1024);
+    int ks = 0, vs = 0;
     const unsigned long long t0 = clock64();
     for (int i = 0; i < iters; ++i) {
       if (SPLIT) {
         pv(0); pv(1); sg(0); sg(1);
+      } else if (COMMITS > 0) {
+        const uint32_t sink = smem_u32(&sink_bar);
+        if (RING) {  // K slots: the three tiles; V slots: the last two
+          dKi = sdesc_add(dK_ring0, ks * TILE);
+          dVi = sdesc_add(dV_ring0, vs * TILE);
+          if (++ks == 3) ks = 0;
+          if (++vs == 2) vs = 0;
+        }
+        wait_ready();
+        wait_ready();
+        wait_ready();
+        pv(0);
+        if (COMMITS >= 4) tc_commit(sink);
+        sg(0);
+        tc_commit(sink);
+        wait_ready();
+        pv(1);
+        if (COMMITS >= 4) tc_commit(sink);
+        sg(1);
+        tc_commit(sink);
       } else {
         pv(0); sg(0); pv(1); sg(1);
       }
@@ -254,13 +296,14 @@ __global__ void __launch_bounds__(384, 1) fwd_stream_kernel(int iters, unsigned 
   }
 }
 
-template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0>
+template <int DPV, bool ALIAS, bool SPLIT, bool BUSY = false, int GAP = 0, int COMMITS = 0, bool WAITS = false,
+          bool RING = false>
 cudaError_t launch_fwd_stream(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
   const int smem = 3 * 128 * 128 * 2 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<DPV, ALIAS, SPLIT, BUSY, GAP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = fwd_stream_kernel<DPV, ALIAS, SPLIT, BUSY, GAP, COMMITS, WAITS, RING>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fwd_stream_kernel<DPV, ALIAS, SPLIT, BUSY, GAP><<<sms, BUSY ? 384 : 128, smem, s>>>(iters, cyc, err);
+  kern<<<sms, BUSY ? 384 : 128, smem, s>>>(iters, cyc, err);
   return cudaGetLastError();
 }
 
@@ -358,6 +401,108 @@ cudaError_t launch_reduce_rate(int sms, const CUtensorMap& tm, float* buf, int r
 
 // Runs one microbenchmark with one CTA per SM and returns the mean over CTAs
 // of (units retired by the CTA) / (its SM cycles).
+// Cycles one thread spends on one synchronisation step, timed with the SM
+// cycle counter around the step and a branch on its result (as a waiting
+// thread consumes it).  KIND 0: mbarrier.try_wait on a completed phase;
+// 1: the same plus tcgen05.fence::after_thread_sync; 2: mbarrier.test_wait on
+// a completed phase; 3: a volatile shared-memory load of a flag;
+// 4: tcgen05.commit; 5: tcgen05.fence::after_thread_sync alone; 6: nothing
+// (the timer's own cost).  With FULL the thread first issues 16 MMAs of the
+// forward kernel's shape, so the step runs while the tensor pipe's queue is
+// full, as it does in the forward kernel's MMA thread.
+template <int KIND, bool FULL>
+__global__ void __launch_bounds__(128, 1) sync_latency_kernel(int iters, unsigned long long* cycles, uint32_t* err) {
+  constexpr int TILE = 128 * 128 * 2;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t ready_bar, sink_bar, done_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gen = smem_raw + (base - raw);
+  for (int i = threadIdx.x; i < 2 * TILE / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gen)[i] =
+        make_uint4(random_bf16x2(4 * i), random_bf16x2(4 * i + 1), random_bf16x2(4 * i + 2), random_bf16x2(4 * i + 3));
+  if (threadIdx.x == 0) {
+    flag = 1;
+    mbar_init(smem_u32(&ready_bar), 1);
+    mbar_init(smem_u32(&sink_bar), 1);
+    mbar_init(smem_u32(&done_bar), 1);
+    fence_mbar_init();
+    mbar_arrive(smem_u32(&ready_bar));
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+    const uint64_t dQ = sdesc_sw128(base, 16, 1024), dK = sdesc_sw128(base + TILE, 16, 1024);
+    const uint32_t ready = smem_u32(&ready_bar), sink = smem_u32(&sink_bar), done = smem_u32(&done_bar);
+    unsigned long long total = 0;
+    uint32_t bad = 0, phase = 0;
+    for (int i = 0; i < iters; ++i) {
+      if (FULL) {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint32_t koff = ((kk % 8) / 4) * (128 * 128) + (kk % 4) * 32;
+          mma_ss(tmem + 128 * (kk / 8), sdesc_add(dQ, koff), sdesc_add(dK, koff), idesc_s, (kk % 8) > 0 ? 1u : 0u);
+        }
+      }
+      const long long t0 = clock64();
+      if constexpr (KIND == 0 || KIND == 1) {
+        if (!mbar_try_wait(ready, 0)) ++bad;
+        if (KIND == 1) tc_fence_after();
+      } else if constexpr (KIND == 2) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(ready), "r"(0u)
+            : "memory");
+        if (!ok) ++bad;
+      } else if constexpr (KIND == 3) {
+        if (flag != 1) ++bad;
+      } else if constexpr (KIND == 4) {
+        tc_commit(sink);
+      } else if constexpr (KIND == 5) {
+        tc_fence_after();
+      }
+      const long long t1 = clock64();
+      total += t1 - t0;
+      if (FULL) {
+        tc_commit(done);
+        if (!wait_drain(done, phase, err, 1000000000ull)) break;
+        phase ^= 1;
+      }
+    }
+    cycles[blockIdx.x] = total + (bad ? 1000000000ull : 0ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int KIND, bool FULL>
+cudaError_t launch_sync_latency(int sms, int iters, unsigned long long* cyc, uint32_t* err, cudaStream_t s) {
+  const int smem = 2 * 128 * 128 * 2 + 1024;
+  auto kern = sync_latency_kernel<KIND, FULL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<sms, 128, smem, s>>>(iters, cyc, err);
+  return cudaGetLastError();
+}
+
 cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -387,6 +532,23 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 18: e = launch_fwd_stream<128, true, false, false, 256>(sms, iters, cyc, err, s); break;
     case 19: e = launch_fwd_stream<128, true, false, false, 600>(sms, iters, cyc, err, s); break;
     case 20: e = launch_fwd_stream<128, true, false, false, 1200>(sms, iters, cyc, err, s); break;
+    case 21: e = launch_fwd_stream<128, true, false, false, 0, 2>(sms, iters, cyc, err, s); break;
+    case 22: e = launch_fwd_stream<128, true, false, false, 0, 4>(sms, iters, cyc, err, s); break;
+    case 23: e = launch_fwd_stream<128, true, false, false, 0, 4, true>(sms, iters, cyc, err, s); break;
+    case 24: e = launch_fwd_stream<128, true, false, false, 0, 4, true, true>(sms, iters, cyc, err, s); break;
+    case 25: e = launch_sync_latency<0, false>(sms, iters, cyc, err, s); break;
+    case 26: e = launch_sync_latency<1, false>(sms, iters, cyc, err, s); break;
+    case 27: e = launch_sync_latency<2, false>(sms, iters, cyc, err, s); break;
+    case 28: e = launch_sync_latency<3, false>(sms, iters, cyc, err, s); break;
+    case 29: e = launch_sync_latency<4, false>(sms, iters, cyc, err, s); break;
+    case 30: e = launch_sync_latency<6, false>(sms, iters, cyc, err, s); break;
+    case 31: e = launch_sync_latency<0, true>(sms, iters, cyc, err, s); break;
+    case 32: e = launch_sync_latency<1, true>(sms, iters, cyc, err, s); break;
+    case 33: e = launch_sync_latency<2, true>(sms, iters, cyc, err, s); break;
+    case 34: e = launch_sync_latency<3, true>(sms, iters, cyc, err, s); break;
+    case 35: e = launch_sync_latency<4, true>(sms, iters, cyc, err, s); break;
+    case 36: e = launch_sync_latency<5, true>(sms, iters, cyc, err, s); break;
+    case 37: e = launch_sync_latency<6, true>(sms, iters, cyc, err, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
@@ -403,6 +565,11 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
   if ((e = cudaMemcpy(host_cyc, cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return e;
   double acc = 0;
+  if (which >= 25) {  // cycles per step, averaged over the SMs
+    for (int i = 0; i < sms; ++i) acc += static_cast<double>(host_cyc[i]) / iters;
+    *result = acc / sms;
+    return cudaSuccess;
+  }
   for (int i = 0; i < sms; ++i) acc += units_per_cta / static_cast<double>(host_cyc[i] ? host_cyc[i] : 1);
   *result = acc / sms;
   return cudaSuccess;

@@ -25,11 +25,28 @@ pytestmark = gpu
     ("fwd_mma_stream_flop_per_sm_clk_d128_gap256", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_d128_gap600", 1024, 32768),
     ("fwd_mma_stream_flop_per_sm_clk_d128_gap1200", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_commit2", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_commit4", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_waits", 1024, 32768),
+    ("fwd_mma_stream_flop_per_sm_clk_d128_waits_ring", 1024, 32768),
     ("tma_reduce_bytes_per_sm_clk", 0.5, 256),
     ("tma_reduce_bytes_per_sm_clk_2slots", 0.5, 256),
     ("red_v4_bytes_per_sm_clk", 0.5, 256),
     ("red_v4_coalesced_bytes_per_sm_clk", 0.5, 256),
     ("tma_and_red_v4_bytes_per_sm_clk", 0.5, 256),
+    ("sync_cycles_try_wait", 0, 5000),
+    ("sync_cycles_try_wait_fence", 0, 5000),
+    ("sync_cycles_test_wait", 0, 5000),
+    ("sync_cycles_flag_load", 0, 5000),
+    ("sync_cycles_commit", 0, 5000),
+    ("sync_cycles_timer", 0, 5000),
+    ("sync_cycles_try_wait_queue_full", 0, 5000),
+    ("sync_cycles_try_wait_fence_queue_full", 0, 5000),
+    ("sync_cycles_test_wait_queue_full", 0, 5000),
+    ("sync_cycles_flag_load_queue_full", 0, 5000),
+    ("sync_cycles_commit_queue_full", 0, 5000),
+    ("sync_cycles_fence_queue_full", 0, 5000),
+    ("sync_cycles_timer_queue_full", 0, 5000),
 ])
 def test_microbench_rates_plausible(name, lo, hi):
     fa = require_gpu()
