@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         for (int t = (nq > C::NSQ ? nq - C::NSQ : 0); t < nq; ++t)
           if (!reduce_tile(t)) break;
       }
-      bulk_wait_group0();   // every reduce has completed before the CTA exits
+      bulk_wait_group_read0();   // every reduce has read its slot; the adds land before the grid ends
       if (*abort_flag) {
         wait_drain(bar(C::B_KV), 0, p.err, p.timeout_ns);
         for (int s = 0; s < C::NSQ && s < fills; ++s) {

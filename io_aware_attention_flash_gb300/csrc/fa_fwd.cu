@@ -400,28 +400,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
         const uint32_t stage = sb + C::OFF_Q + t * C::TILE_BYTES;
         uint16_t* orow = p.o + (static_cast<size_t>(sp.row_base + q_row) * p.sv.H + sp.h) * D;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 16; ++ch) {  // 16 columns (two 16-byte chunks) at a time
-          uint32_t o[16];
-          tmem_ld16(tO + ch * 16, o);
+        for (int cb = 0; cb < D / 64; ++cb) {  // 64 columns (one 128-byte swizzle block) per TMEM round trip
+          uint32_t o[2][32];
+          tmem_ld32(tO + cb * 64, o[0]);
+          tmem_ld32(tO + cb * 64 + 32, o[1]);
           tmem_wait_ld();
-          reg_fence(o);
-          uint32_t w[8];
+          reg_fence(o[0]);
+          reg_fence(o[1]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-          if (via_tma) {
-            const uint32_t rowaddr = stage + (ch / 4) * C::BLK_BYTES + r * 128;
+          for (int ch = 0; ch < 4; ++ch) {  // 16 columns (two 16-byte chunks) at a time
+            uint32_t w[8];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const uint32_t chunk = ((ch % 4) * 2 + u) ^ (r & 7);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + chunk * 16), "r"(w[4 * u]),
-                           "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
-                           : "memory");
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[ch / 2][(ch % 2) * 16 + 2 * e]) * inv_l,
+                                 __uint_as_float(o[ch / 2][(ch % 2) * 16 + 2 * e + 1]) * inv_l);
+            if (via_tma) {
+              const uint32_t rowaddr = stage + cb * C::BLK_BYTES + r * 128;
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const uint32_t chunk = (ch * 2 + u) ^ (r & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + chunk * 16), "r"(w[4 * u]),
+                             "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                             : "memory");
+              }
+            } else if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cb * 64 + ch * 16);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
-          } else if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
         }
         if (store) {
@@ -436,7 +442,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
             for (int kb = 0; kb < C::KB; ++kb)
               tma_store_4d(&tmO, stage + kb * C::BLK_BYTES, kb * 64, sp.h, sp.tma_row0 + qt, sp.tma_b);
             bulk_commit_group();
-            bulk_wait_group0();   // the copies are complete before the CTA exits
+            // The stage may be released once the copies have read it; their
+            // global writes complete before the grid does.
+            bulk_wait_group_read0();
           }
         }
       }
