@@ -227,6 +227,10 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *              timer alone
  *          31..37: 25..29, the fence alone, and the timer alone, each right
  *              after the thread issued 16 MMAs (tensor queue full)
+ *          38..41: exponentials per SM per clock in the softmax's per-pair
+ *              step: 38 two ex2 + one cvt.rn.bf16x2.f32, 39 two ex2 + an
+ *              integer bf16 pack, 40 the forward softmax's full step (paired
+ *              FMA, ex2, paired add, cvt pack), 41 step 40 with the integer pack
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

@@ -21,12 +21,21 @@ constexpr int kMaxSms = 1024;
 __device__ unsigned long long g_cycles[kMaxSms];
 __device__ float g_sink[kMaxSms];
 
-// kind 0: ex2.approx.ftz.f32; 1: cvt.rn.bf16x2.f32; 2: fma.rn.f32.
+// kind 0: ex2.approx.ftz.f32; 1: cvt.rn.bf16x2.f32; 2: fma.rn.f32.  The
+// softmax's per-pair step, counted in exponentials: 3: two ex2 and one
+// cvt.rn.bf16x2.f32; 4: two ex2 and a bf16 pack by integer rounding (add
+// 0x8000, keep the high halves); 5: the forward softmax's full step (paired
+// FMA, two ex2, paired add into a row sum, cvt pack); 6: kind 5 with the
+// integer pack of kind 4.
 template <int KIND>
 __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned long long* cycles, float* sink) {
   float x[kChains];
 #pragma unroll
   for (int c = 0; c < kChains; ++c) x[c] = -1.0f - 0.001f * (threadIdx.x + c);
+  uint64_t acc2[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) acc2[c] = f2_pack(0.f, 0.f);
+  const uint64_t c2 = f2_pack(0.9f, 0.9f), n2 = f2_pack(-0.1f, -0.2f);
   __syncthreads();
   const unsigned long long t0 = clock64();
   for (int i = 0; i < iters; ++i) {
@@ -37,6 +46,17 @@ __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned 
       } else if constexpr (KIND == 1) {
         const uint32_t p = pack_bf16x2(x[c], x[c] + 1.0f);
         x[c] = __uint_as_float(p & 0xFFFF0000u) * 0.5f - 0.75f;
+      } else if constexpr (KIND >= 3) {
+        float x0 = x[c], x1 = x[c] - 0.25f;
+        if constexpr (KIND >= 5) f2_unpack(ffma2(f2_pack(x0, x1), c2, n2), x0, x1);
+        const float a = ex2_approx(x0), b = ex2_approx(x1);
+        if constexpr (KIND >= 5) acc2[c] = fadd2(acc2[c], f2_pack(a, b));
+        uint32_t pk;
+        if constexpr (KIND == 3 || KIND == 5)
+          pk = pack_bf16x2(a, b);
+        else
+          pk = __byte_perm(__float_as_uint(a) + 0x8000u, __float_as_uint(b) + 0x8000u, 0x7632);
+        x[c] = __uint_as_float(pk & 0xFFFF0000u) * -0.5f - 0.75f;  // stays in (-1.2, -0.8)
       } else {
         x[c] = fmaf(x[c], 0.999f, -0.001f);
       }
@@ -46,7 +66,11 @@ __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned 
   const unsigned long long t1 = clock64();
   float s = 0.f;
 #pragma unroll
-  for (int c = 0; c < kChains; ++c) s += x[c];
+  for (int c = 0; c < kChains; ++c) {
+    float a0, a1;
+    f2_unpack(acc2[c], a0, a1);
+    s += x[c] + a0 + a1;
+  }
   if (s == 12345.f) sink[threadIdx.x % kMaxSms] = s;  // keeps the loop alive
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
@@ -519,6 +543,10 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 0: unit_rate_kernel<0><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 1: unit_rate_kernel<1><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 2: unit_rate_kernel<2><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 38: unit_rate_kernel<3><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 39: unit_rate_kernel<4><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 40: unit_rate_kernel<5><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 41: unit_rate_kernel<6><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 3: e = launch_mma_rate<256, false, false>(sms, iters, cyc, err, s); break;
     case 4: e = launch_mma_rate<128, false, false>(sms, iters, cyc, err, s); break;
     case 5: e = launch_mma_rate<128, true, false>(sms, iters, cyc, err, s); break;
@@ -554,6 +582,8 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
   if (e != cudaSuccess) return e;
   if (which <= 2)
     units_per_cta = static_cast<double>(threads) * iters * kChains;
+  else if (which >= 38)  // two exponentials per step
+    units_per_cta = 2.0 * threads * iters * kChains;
   else if (which <= 7)
     units_per_cta = 2.0 * 128 * ((which == 3 || which == 6) ? 256 : 128) * 64 * static_cast<double>(iters);
   else  // two query tiles x (S: 128 x 128 x 128, PV: 128 x DPV x 128)
@@ -565,7 +595,7 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
   if ((e = cudaMemcpy(host_cyc, cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return e;
   double acc = 0;
-  if (which >= 25) {  // cycles per step, averaged over the SMs
+  if (which >= 25 && which <= 37) {  // cycles per step, averaged over the SMs
     for (int i = 0; i < sms; ++i) acc += static_cast<double>(host_cyc[i]) / iters;
     *result = acc / sms;
     return cudaSuccess;

@@ -12,6 +12,10 @@ pytestmark = gpu
     ("ex2_per_sm_clk", 4, 256),
     ("cvt_bf16x2_per_sm_clk", 4, 256),
     ("ffma_per_sm_clk", 32, 256),
+    ("softmax_ex2_cvt_per_sm_clk", 4, 256),
+    ("softmax_ex2_intpack_per_sm_clk", 4, 256),
+    ("softmax_step_per_sm_clk", 4, 256),
+    ("softmax_step_intpack_per_sm_clk", 4, 256),
     ("mma_bf16_flop_per_sm_clk_n256", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a", 1024, 32768),
