@@ -8,12 +8,15 @@
 //
 //   fa_decode_split_kernel  persistent (one CTA per SM); CTA c takes work items
 //                           c, c + G, ... where item = (sequence·head, split).
-//                           Warp 4 streams the 128-key K and V tiles of its
-//                           items through a 3-stage TMA ring without draining
-//                           between items; warps 0-3 each own 32 keys of every
-//                           tile and keep their own partial softmax (so the
-//                           four warps never synchronise with each other) and
-//                           write one partial (m, l, O) per item.
+//                           The last warp streams the 128-key K and V tiles of
+//                           its items through a 3-stage TMA ring without
+//                           draining between items; compute warp w owns keys
+//                           32·(w mod 4) .. +31 of every tile and a group of
+//                           the queries (with two or more queries, two groups:
+//                           two warps per SM sub-partition share the keys) and
+//                           keeps its own partial softmax (the compute warps
+//                           never synchronise with each other), writing one
+//                           partial (m, l, O) per item, key quarter and query.
 //   fa_decode_merge_kernel  one warp per (sequence, head, query): combines the
 //                           4·S partials into O (bf16) and LSE.
 //
@@ -32,7 +35,7 @@
 namespace fa {
 namespace {
 
-template <int D>
+template <int D, int QG>
 struct DecCfg {
   static constexpr int KB = D / 64;                    // 128-byte swizzle blocks per row
   static constexpr int BLK_BYTES = kTile * 128;        // 128 rows x 64 bf16
@@ -42,15 +45,16 @@ struct DecCfg {
   static constexpr int E = D / 32;                     // head-dimension elements per lane
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
-  static constexpr int OFF_P = OFF_V + NST * TILE_BYTES;  // [4 warps][NQMAX][32] fp32 probabilities
-  static constexpr int OFF_BAR = OFF_P + 4 * NQMAX * 32 * 4;
+  static constexpr int NCW = 4 * QG;                   // compute warps: 4 key quarters x QG query groups
+  static constexpr int OFF_P = OFF_V + NST * TILE_BYTES;  // [NCW][NQMAX][32] fp32 probabilities
+  static constexpr int OFF_BAR = OFF_P + NCW * NQMAX * 32 * 4;
   static constexpr int B_FULL = 0;
   static constexpr int B_EMPTY = NST;
   static constexpr int NBAR = 2 * NST;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
-  static constexpr int NUM_THREADS = 160;              // warps 0-3 compute, warp 4 TMA
+  static constexpr int NUM_THREADS = 32 * (NCW + 1);   // compute warps, then the TMA warp
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -97,11 +101,13 @@ __device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
   }
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
+template <int D, int NQ, int QG>
+__global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            const DecodeParams p) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, QG>;
+  static_assert(NQ % QG == 0, "queries split evenly over the query groups");
+  constexpr int NQW = NQ / QG;  // queries per compute warp
   constexpr int E = C::E;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -114,10 +120,10 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int n_items = p.B * p.H * p.splits;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == C::NCW && lane == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_FULL + s), 1);
-      mbar_init(bar(C::B_EMPTY + s), 128);
+      mbar_init(bar(C::B_EMPTY + s), C::NCW * 32);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
   }
   __syncthreads();
 
-  if (warp == 4) {
+  if (warp == C::NCW) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
@@ -163,6 +169,8 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
   } else {
     // ---------------------------------------------------------------- scores, softmax, P·V
     const float c = p.scale_log2;
+    const int kw = warp % 4;          // key quarter of every tile
+    const int q0 = (warp / 4) * NQW;  // first query of this warp's group
     float* pbuf = reinterpret_cast<float*>(smem + C::OFF_P) + warp * C::NQMAX * 32;
     int t = 0;  // tiles consumed
     bool ok = true;
@@ -170,10 +178,10 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
       const int bh = item / p.splits, split = item - (item / p.splits) * p.splits;
       const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
       const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
-      float qv[NQ][E], o[NQ][E], m[NQ], lp[NQ];
+      float qv[NQW][E], o[NQW][E], m[NQW], lp[NQW];
 #pragma unroll
-      for (int qq = 0; qq < NQ; ++qq) {
-        const int qi = qq < p.Nq ? qq : 0;
+      for (int qq = 0; qq < NQW; ++qq) {
+        const int qi = q0 + qq < p.Nq ? q0 + qq : 0;
         const uint16_t* qrow = p.q + ((static_cast<size_t>(b) * p.Nq + qi) * p.H + h) * D + E * lane;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -191,12 +199,12 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
         }
         const uint32_t ktile = sb + C::OFF_K + st * C::TILE_BYTES;
         const uint32_t vtile = sb + C::OFF_V + st * C::TILE_BYTES;
-        const int key = kt + warp * 32 + lane;  // this lane's key after the reduction
+        const int key = kt + kw * 32 + lane;  // this lane's key after the reduction
         // ---- scores of this warp's 32 keys, one query at a time (not unrolled:
         // one set of 32 partial dot products live at a time)
-        float sc[NQ];
+        float sc[NQW];
 #pragma unroll 1
-        for (int qq = 0; qq < NQ; ++qq) {
+        for (int qq = 0; qq < NQW; ++qq) {
           float qcur[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) qcur[e] = qv[qq][e];
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < 32; ++kk) {
             float kx[E];
-            load_row_slice<D>(ktile + row_slice<D>(warp * 32 + kk, lane), kx);
+            load_row_slice<D>(ktile + row_slice<D>(kw * 32 + kk, lane), kx);
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) acc = fmaf(qcur[e], kx[e], acc);
@@ -213,12 +221,12 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
           transpose_reduce32(part, lane);
           // Causal: the new tokens are the last Nq positions, so query qq sees
           // keys up to Nk - Nq + qq.
-          const int lim = p.causal ? p.Nk - p.Nq + qq : p.Nk - 1;
-          sc[qq] = (qq < p.Nq && key <= lim && key < p.Nk) ? part[0] * c : -CUDART_INF_F;
+          const int lim = p.causal ? p.Nk - p.Nq + q0 + qq : p.Nk - 1;
+          sc[qq] = (q0 + qq < p.Nq && key <= lim && key < p.Nk) ? part[0] * c : -CUDART_INF_F;
         }
         // ---- online softmax over the warp's keys, per query
 #pragma unroll
-        for (int qq = 0; qq < NQ; ++qq) {
+        for (int qq = 0; qq < NQW; ++qq) {
           float mt = sc[qq];
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
@@ -236,9 +244,9 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
 #pragma unroll 4
         for (int kk = 0; kk < 32; ++kk) {
           float vx[E];
-          load_row_slice<D>(vtile + row_slice<D>(warp * 32 + kk, lane), vx);
+          load_row_slice<D>(vtile + row_slice<D>(kw * 32 + kk, lane), vx);
 #pragma unroll
-          for (int qq = 0; qq < NQ; ++qq) {
+          for (int qq = 0; qq < NQW; ++qq) {
             const float pq = pbuf[qq * 32 + kk];
 #pragma unroll
             for (int e = 0; e < E; ++e) o[qq][e] = fmaf(pq, vx[e], o[qq][e]);
@@ -249,19 +257,19 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
       }
       if (!ok) break;
       // ---- this warp's partial for the item: (m, l, unnormalised O) per query
-      const size_t part_idx = static_cast<size_t>(item) * 4 + warp;
+      const size_t part_idx = static_cast<size_t>(item) * 4 + kw;
 #pragma unroll
-      for (int qq = 0; qq < NQ; ++qq) {
-        if (qq >= p.Nq) break;
+      for (int qq = 0; qq < NQW; ++qq) {
+        if (q0 + qq >= p.Nq) break;
         float l = lp[qq];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        float* op = p.o_part + (part_idx * p.Nq + qq) * D + E * lane;
+        float* op = p.o_part + (part_idx * p.Nq + q0 + qq) * D + E * lane;
 #pragma unroll
         for (int e = 0; e < E; ++e) op[e] = o[qq][e];
         if (lane == 0) {
-          p.ml_part[(part_idx * p.Nq + qq) * 2 + 0] = m[qq];
-          p.ml_part[(part_idx * p.Nq + qq) * 2 + 1] = l;
+          p.ml_part[(part_idx * p.Nq + q0 + qq) * 2 + 0] = m[qq];
+          p.ml_part[(part_idx * p.Nq + q0 + qq) * 2 + 1] = l;
         }
       }
     }
@@ -309,18 +317,23 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams
     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Nq + qq] = l > 0.f ? (mmax + log2f(l)) * kLn2 : -CUDART_INF_F;
 }
 
+// Two query groups whenever there are two or more queries: two warps per SM
+// sub-partition then share each key quarter (one warp per sub-partition is
+// issue bound once it carries several queries; four groups measured no
+// faster, as every group re-reads the K tile from shared memory).
 template <int D, int NQ>
 cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                              cudaStream_t s) {
-  using C = DecCfg<D>;
+  constexpr int QG = NQ >= 2 ? 2 : 1;
+  using C = DecCfg<D, QG>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_split_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_split_kernel<D, NQ, QG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  fa_decode_split_kernel<D, NQ><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
+  fa_decode_split_kernel<D, NQ, QG><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
