@@ -231,6 +231,10 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *              step: 38 two ex2 + one cvt.rn.bf16x2.f32, 39 two ex2 + an
  *              integer bf16 pack, 40 the forward softmax's full step (paired
  *              FMA, ex2, paired add, cvt pack), 41 step 40 with the integer pack
+ *          42: largest relative difference of the polynomial exp2 (FMA pipe)
+ *              from ex2.approx over [-30, 8]; -1 if a clamped input gave a
+ *              negative, NaN or non-tiny value
+ *          43: step 40 with a quarter of the pairs through the polynomial exp2
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

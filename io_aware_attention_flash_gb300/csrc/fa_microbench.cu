@@ -4,8 +4,10 @@
 // many bf16 FLOPs tcgen05.mma retires.  Each kernel times itself with the SM
 // cycle counter, so the results are in units per SM-clock whatever the clock.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math_constants.h>
 
 #include "fa_kernels.cuh"
 #include "ptx.cuh"
@@ -26,7 +28,8 @@ __device__ float g_sink[kMaxSms];
 // cvt.rn.bf16x2.f32; 4: two ex2 and a bf16 pack by integer rounding (add
 // 0x8000, keep the high halves); 5: the forward softmax's full step (paired
 // FMA, two ex2, paired add into a row sum, cvt pack); 6: kind 5 with the
-// integer pack of kind 4.
+// integer pack of kind 4; 7: kind 5 with a quarter of the pairs through the
+// polynomial exp2 (ex2_poly2) instead of the special-function unit.
 template <int KIND>
 __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned long long* cycles, float* sink) {
   float x[kChains];
@@ -49,10 +52,16 @@ __global__ void __launch_bounds__(1024, 1) unit_rate_kernel(int iters, unsigned 
       } else if constexpr (KIND >= 3) {
         float x0 = x[c], x1 = x[c] - 0.25f;
         if constexpr (KIND >= 5) f2_unpack(ffma2(f2_pack(x0, x1), c2, n2), x0, x1);
-        const float a = ex2_approx(x0), b = ex2_approx(x1);
+        float a, b;
+        if (KIND == 7 && (c & 3) == 3) {
+          f2_unpack(ex2_poly2(x0, x1), a, b);
+        } else {
+          a = ex2_approx(x0);
+          b = ex2_approx(x1);
+        }
         if constexpr (KIND >= 5) acc2[c] = fadd2(acc2[c], f2_pack(a, b));
         uint32_t pk;
-        if constexpr (KIND == 3 || KIND == 5)
+        if constexpr (KIND == 3 || KIND == 5 || KIND == 7)
           pk = pack_bf16x2(a, b);
         else
           pk = __byte_perm(__float_as_uint(a) + 0x8000u, __float_as_uint(b) + 0x8000u, 0x7632);
@@ -84,6 +93,25 @@ __device__ __forceinline__ uint32_t random_bf16x2(uint32_t i) {
   const uint32_t lo = (h & 0x8000u) | 0x3F00u | (h & 0x7Fu);
   const uint32_t hi = ((h >> 16) & 0x8000u) | 0x3F00u | ((h >> 16) & 0x7Fu);
   return lo | (hi << 16);
+}
+
+// Accuracy of ex2_poly2 against ex2.approx.ftz.f32 over x in [-30, 8]
+// (2^20 points): the largest relative difference, as fp32 bits in *out (a
+// positive float orders as its bits).  Inputs far below the clamp (-1e4,
+// -inf) must give a value in [0, 2^-100]; otherwise *bad is set.
+__global__ void ex2_poly_accuracy_kernel(unsigned int* out, unsigned int* bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const float x0 = -30.0f + 38.0f * (static_cast<float>(i) / 1048576.0f);
+  const float x1 = -30.0f + 38.0f * (static_cast<float>(i) + 0.5f) / 1048576.0f;
+  float p0, p1;
+  f2_unpack(ex2_poly2(x0, x1), p0, p1);
+  const float e0 = fabsf(p0 / ex2_approx(x0) - 1.0f), e1 = fabsf(p1 / ex2_approx(x1) - 1.0f);
+  atomicMax(out, __float_as_uint(fmaxf(e0, e1)));
+  if (i == 0) {
+    float q0, q1;
+    f2_unpack(ex2_poly2(-1.0e4f, -CUDART_INF_F), q0, q1);
+    if (!(q0 >= 0.0f && q0 <= 7.9e-31f && q1 >= 0.0f && q1 <= 7.9e-31f)) atomicOr(bad, 1u);
+  }
 }
 
 // tcgen05.mma throughput: one thread issues `iters` x 4 MMAs of M=128, N, K=16
@@ -547,6 +575,20 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 39: unit_rate_kernel<4><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 40: unit_rate_kernel<5><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 41: unit_rate_kernel<6><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 43: unit_rate_kernel<7><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 42: {  // accuracy, not a rate
+      unsigned int* acc = reinterpret_cast<unsigned int*>(cyc);
+      if ((e = cudaMemsetAsync(acc, 0, 2 * sizeof(unsigned int), s)) != cudaSuccess) return e;
+      ex2_poly_accuracy_kernel<<<4096, 256, 0, s>>>(acc, acc + 1);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      unsigned int h[2];
+      if ((e = cudaMemcpyAsync(h, acc, sizeof(h), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return e;
+      if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+      float r;
+      memcpy(&r, &h[0], sizeof(r));
+      *result = h[1] ? -1.0 : static_cast<double>(r);
+      return cudaSuccess;
+    }
     case 3: e = launch_mma_rate<256, false, false>(sms, iters, cyc, err, s); break;
     case 4: e = launch_mma_rate<128, false, false>(sms, iters, cyc, err, s); break;
     case 5: e = launch_mma_rate<128, true, false>(sms, iters, cyc, err, s); break;
@@ -582,7 +624,7 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
   if (e != cudaSuccess) return e;
   if (which <= 2)
     units_per_cta = static_cast<double>(threads) * iters * kChains;
-  else if (which >= 38)  // two exponentials per step
+  else if (which >= 38)  // two exponentials per step (38-41, 43)
     units_per_cta = 2.0 * threads * iters * kChains;
   else if (which <= 7)
     units_per_cta = 2.0 * 128 * ((which == 3 || which == 6) ? 256 : 128) * 64 * static_cast<double>(iters);

@@ -372,6 +372,33 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 }
 // max(a, b, c) in one instruction (sm_100 and later); same result as two
 // fmaxf for non-NaN inputs.
+// 2^x for a pair of floats without the special-function unit (FMA and
+// integer pipes only), for offloading part of a softmax's exponentials
+// ("LLM Systems 22", section 4.2.1: exponentials emulated by a polynomial).
+// Range reduction: x = n + f, n = round(x) by adding 1.5·2^23 (the sum's low
+// mantissa bits hold n), f in [-0.5, 0.5]; 2^f by a cubic whose coefficients
+// were fitted for this project (iteratively reweighted least squares on the
+// relative error over [-0.5, 0.5]: max relative error 7.5e-5, evaluated in
+// fp32, far below bf16's 2^-9); n is then added to the exponent field.  x is
+// clamped to >= -126 (results below 2^-126 come out as tiny or zero values,
+// never negative or NaN); x must be <= 127.
+__device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  const uint64_t x2 = f2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+  const uint64_t shift2 = f2_pack(kShift, kShift);
+  const uint64_t t2 = fadd2(x2, shift2);
+  const uint64_t f2 = fsub2(x2, fsub2(t2, shift2));
+  uint64_t p2 = ffma2(f2_pack(0.05517132f, 0.05517132f), f2, f2_pack(0.24261054f, 0.24261054f));
+  p2 = ffma2(p2, f2, f2_pack(0.69326097f, 0.69326097f));
+  p2 = ffma2(p2, f2, f2_pack(0.99992812f, 0.99992812f));
+  float t0, t1, p0, p1;
+  f2_unpack(t2, t0, t1);
+  f2_unpack(p2, p0, p1);
+  const uint32_t r0 = __float_as_uint(p0) + (__float_as_uint(t0) << 23);
+  const uint32_t r1 = __float_as_uint(p1) + (__float_as_uint(t1) << 23);
+  return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -16,6 +16,8 @@ pytestmark = gpu
     ("softmax_ex2_intpack_per_sm_clk", 4, 256),
     ("softmax_step_per_sm_clk", 4, 256),
     ("softmax_step_intpack_per_sm_clk", 4, 256),
+    ("softmax_step_quarter_poly_per_sm_clk", 4, 256),
+    ("ex2_poly_max_rel_err", 0, 1e-4),
     ("mma_bf16_flop_per_sm_clk_n256", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a", 1024, 32768),
