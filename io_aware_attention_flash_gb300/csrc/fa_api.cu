@@ -289,7 +289,7 @@ void decode_split(int B, int H, int Nk, int* splits, int* split_len) {
 size_t decode_ws_bytes(int B, int H, int Nq, int Nk, int d) {
   int splits = 0, split_len = 0;
   decode_split(B, H, Nk, &splits, &split_len);
-  const size_t parts = static_cast<size_t>(B) * H * splits * 4 * Nq;
+  const size_t parts = static_cast<size_t>(B) * H * splits * Nq;
   return pad256(parts * d * 4) + pad256(parts * 2 * 4);
 }
 
@@ -402,7 +402,7 @@ FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   decode_split(B, H, Nk, &p.splits, &p.split_len);
-  const size_t parts = static_cast<size_t>(B) * H * p.splits * 4 * Nq;
+  const size_t parts = static_cast<size_t>(B) * H * p.splits * Nq;
   p.o_part = static_cast<float*>(workspace);
   p.ml_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pad256(parts * d * 4));
   p.B = B;

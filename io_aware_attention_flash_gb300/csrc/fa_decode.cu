@@ -15,10 +15,12 @@
 //                           the queries (with two or more queries, two groups:
 //                           two warps per SM sub-partition share the keys) and
 //                           keeps its own partial softmax (the compute warps
-//                           never synchronise with each other), writing one
-//                           partial (m, l, O) per item, key quarter and query.
+//                           do not synchronise within an item); at the end of
+//                           an item the four key quarters' partials are
+//                           combined in shared memory into one partial
+//                           (m, l, O) per item and query.
 //   fa_decode_merge_kernel  one warp per (sequence, head, query): combines the
-//                           4·S partials into O (bf16) and LSE.
+//                           S partials into O (bf16) and LSE.
 //
 // The bytes are the cost (K and V once, 4·d bytes per cached token and head),
 // so the arithmetic runs on the FMA pipe: lanes split the head dimension for
@@ -47,10 +49,16 @@ struct DecCfg {
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
   static constexpr int NCW = 4 * QG;                   // compute warps: 4 key quarters x QG query groups
   static constexpr int OFF_P = OFF_V + NST * TILE_BYTES;  // [NCW][NQMAX][32] fp32 probabilities
-  static constexpr int OFF_BAR = OFF_P + NCW * NQMAX * 32 * 4;
+  // [QG][4 key quarters][NQMAX / QG queries][D + 2] fp32: each warp's (O, m, l)
+  // of an item, combined into one partial per query group by its first warp.
+  static constexpr int CMB_STRIDE = D + 2;
+  static constexpr int OFF_CMB = OFF_P + NCW * NQMAX * 32 * 4;
+  static constexpr int OFF_BAR = OFF_CMB + 4 * NQMAX * CMB_STRIDE * 4;
   static constexpr int B_FULL = 0;
   static constexpr int B_EMPTY = NST;
-  static constexpr int NBAR = 2 * NST;
+  static constexpr int B_CFULL = 2 * NST;        // [QG]: a group's four partials are in shared memory
+  static constexpr int B_CFREE = 2 * NST + QG;   // [QG]: the group's first warp has read them
+  static constexpr int NBAR = 2 * NST + 2 * QG;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -125,6 +133,10 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
       mbar_init(bar(C::B_FULL + s), 1);
       mbar_init(bar(C::B_EMPTY + s), C::NCW * 32);
     }
+    for (int g = 0; g < QG; ++g) {
+      mbar_init(bar(C::B_CFULL + g), 4 * 32);
+      mbar_init(bar(C::B_CFREE + g), 32);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -170,7 +182,10 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
     // ---------------------------------------------------------------- scores, softmax, P·V
     const float c = p.scale_log2;
     const int kw = warp % 4;          // key quarter of every tile
-    const int q0 = (warp / 4) * NQW;  // first query of this warp's group
+    const int qg = warp / 4;          // query group
+    const int q0 = qg * NQW;          // first query of this warp's group
+    float* cmb = reinterpret_cast<float*>(smem + C::OFF_CMB) + qg * 4 * NQW * C::CMB_STRIDE;
+    int n_done = 0;                   // items this warp has finished
     float* pbuf = reinterpret_cast<float*>(smem + C::OFF_P) + warp * C::NQMAX * 32;
     int t = 0;  // tiles consumed
     bool ok = true;
@@ -256,37 +271,80 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
         mbar_arrive(bar(C::B_EMPTY + st));
       }
       if (!ok) break;
-      // ---- this warp's partial for the item: (m, l, unnormalised O) per query
-      const size_t part_idx = static_cast<size_t>(item) * 4 + kw;
+      // ---- the item's partial (m, l, unnormalised O) per query: the four key
+      // quarters' partials meet in shared memory and the group's first warp
+      // combines them (bounded mbarrier waits, so an abort cannot strand a warp).
+      if (kw != 0 && n_done > 0 &&
+          !wait_bounded(bar(C::B_CFREE + qg), (n_done - 1) & 1, abort_flag, p.err, p.timeout_ns))
+        break;
 #pragma unroll
       for (int qq = 0; qq < NQW; ++qq) {
-        if (q0 + qq >= p.Nq) break;
         float l = lp[qq];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        float* op = p.o_part + (part_idx * p.Nq + q0 + qq) * D + E * lane;
+        float* row = cmb + (kw * NQW + qq) * C::CMB_STRIDE;
 #pragma unroll
-        for (int e = 0; e < E; ++e) op[e] = o[qq][e];
+        for (int e = 0; e < E; ++e) row[E * lane + e] = o[qq][e];
         if (lane == 0) {
-          p.ml_part[(part_idx * p.Nq + q0 + qq) * 2 + 0] = m[qq];
-          p.ml_part[(part_idx * p.Nq + q0 + qq) * 2 + 1] = l;
+          row[D] = m[qq];
+          row[D + 1] = l;
         }
       }
+      mbar_arrive(bar(C::B_CFULL + qg));
+      if (kw == 0) {
+        if (!wait_bounded(bar(C::B_CFULL + qg), n_done & 1, abort_flag, p.err, p.timeout_ns)) break;
+#pragma unroll
+        for (int qq = 0; qq < NQW; ++qq) {
+          if (q0 + qq >= p.Nq) break;
+          float mk[4], mx = -CUDART_INF_F;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mk[k] = cmb[(k * NQW + qq) * C::CMB_STRIDE + D];
+            mx = fmaxf(mx, mk[k]);
+          }
+          float acc[E], l = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (mk[k] == -CUDART_INF_F) continue;
+            const float* row = cmb + (k * NQW + qq) * C::CMB_STRIDE;
+            const float w = ex2_approx(mk[k] - mx);
+            l = fmaf(w, row[D + 1], l);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, row[E * lane + e], acc[e]);
+          }
+          const size_t idx = static_cast<size_t>(item) * p.Nq + q0 + qq;
+          float* op = p.o_part + idx * D + E * lane;
+#pragma unroll
+          for (int e = 0; e < E; ++e) op[e] = acc[e];
+          if (lane == 0) {
+            p.ml_part[idx * 2 + 0] = mx;
+            p.ml_part[idx * 2 + 1] = l;
+          }
+        }
+        __syncwarp();
+        mbar_arrive(bar(C::B_CFREE + qg));
+      }
+      ++n_done;
     }
   }
 }
 
 // One warp per (sequence, head, query): O = Σ 2^(m_p − m) O_p / Σ 2^(m_p − m) l_p
-// over the 4·splits partials of the head, m = max m_p; LSE = ln 2 · (m + log2 l).
+// over the splits partials of the head, m = max m_p; LSE = ln 2 · (m + log2 l).
+// The partials' weights are formed 32 at a time, one per lane, and the O
+// partials are then read with several loads in flight (no load waits on
+// another).
 template <int D>
-__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(64) fa_decode_merge_kernel(const DecodeParams p) {
   constexpr int E = D / 32;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= p.B * p.H * p.Nq) return;
   const int qq = wid % p.Nq, bh = wid / p.Nq;
   const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
-  const int n_part = 4 * p.splits;
+  const int n_part = p.splits;
   const size_t part0 = static_cast<size_t>(bh) * n_part;
   float mmax = -CUDART_INF_F;
   for (int i = lane; i < n_part; i += 32) mmax = fmaxf(mmax, p.ml_part[((part0 + i) * p.Nq + qq) * 2]);
@@ -297,16 +355,37 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float l = 0.f;
   if (mmax != -CUDART_INF_F) {
-    for (int i = 0; i < n_part; ++i) {
-      const size_t idx = (part0 + i) * p.Nq + qq;
-      const float mp = p.ml_part[idx * 2];
-      if (mp == -CUDART_INF_F) continue;
-      const float w = ex2_approx(mp - mmax);
-      l = fmaf(w, p.ml_part[idx * 2 + 1], l);
-      const float* op = p.o_part + idx * D + E * lane;
+    for (int i0 = 0; i0 < n_part; i0 += 32) {
+      float w = 0.f;  // this lane's partial: i0 + lane
+      if (i0 + lane < n_part) {
+        const size_t idx = (part0 + i0 + lane) * p.Nq + qq;
+        const float mp = p.ml_part[idx * 2];
+        if (mp != -CUDART_INF_F) {
+          w = ex2_approx(mp - mmax);
+          l = fmaf(w, p.ml_part[idx * 2 + 1], l);
+        }
+      }
+      const int cnt = min(32, n_part - i0);
+#pragma unroll 8
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const float* op = p.o_part + ((part0 + i0 + j) * p.Nq + qq) * D + E * lane;
+        float v[E];
+        if constexpr (E == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(op);
+          v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(op);
+          v[0] = t.x, v[1] = t.y;
+        }
+        if (wj != 0.f) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, op[e], acc[e]);
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+        }
+      }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   }
   const float inv_l = l > 0.f ? 1.0f / l : 0.f;
   uint16_t* orow = p.o + ((static_cast<size_t>(b) * p.Nq + qq) * p.H + h) * D + E * lane;
@@ -317,10 +396,6 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecodeParams
     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Nq + qq] = l > 0.f ? (mmax + log2f(l)) * kLn2 : -CUDART_INF_F;
 }
 
-// Two query groups whenever there are two or more queries: two warps per SM
-// sub-partition then share each key quarter (one warp per sub-partition is
-// issue bound once it carries several queries; four groups measured no
-// faster, as every group re-reads the K tile from shared memory).
 template <int D, int NQ>
 cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                              cudaStream_t s) {
@@ -337,7 +412,8 @@ cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
-  fa_decode_merge_kernel<D><<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(p);
+  // Two warps per block: the rows are few (B·H·Nq), so spread them over the SMs.
+  fa_decode_merge_kernel<D><<<static_cast<unsigned>((warps * 32 + 63) / 64), 64, 0, s>>>(p);
   return cudaGetLastError();
 }
 
