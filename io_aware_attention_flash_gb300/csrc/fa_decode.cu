@@ -331,6 +331,306 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Several new tokens (d = 128): the two products of each 128-key tile on the
+// tensor core, with the keys as the M dimension and the queries as N = 16
+// (rows past Nq are zero):
+//   Sᵀ = K · Qᵀ      A = K tile (K-major), B = Q (16 x d, K-major)  -> TMEM, 16 cols
+//   Oᵀ_tile = Vᵀ · Pᵀ  A = V tile read MN-major, B = P (16 x 128 keys, K-major)
+// Thread t of warps 0-3 owns TMEM lane t: key t of the tile for Sᵀ and P,
+// head dimension t for Oᵀ.  The online softmax runs per query across the four
+// warps (tile maxima exchanged through shared memory behind a bounded
+// mbarrier); each thread keeps its key's partial row sums and its dimension's
+// running output in registers, so the tensor memory holds only per-tile
+// results (Sᵀ and Oᵀ_tile, double-buffered: 64 columns).  Warp 4 streams
+// K and V through the same 3-stage TMA ring as the FMA kernel; warp 5 issues
+// the MMAs.  One partial (m, l, O) per item and query, merged as above.
+// ----------------------------------------------------------------------------
+struct DecMmaCfg {
+  static constexpr int D = 128;
+  static constexpr int NQP = 16;                        // queries padded to the MMA's N
+  static constexpr int BLK_BYTES = kTile * 128;         // 128 rows x 64 bf16
+  static constexpr int TILE_BYTES = 2 * BLK_BYTES;      // 128 keys x 128
+  static constexpr int QBLK = NQP * 128;                // 16 rows x 64 bf16
+  static constexpr int NST = 3;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
+  static constexpr int OFF_Q = OFF_V + NST * TILE_BYTES;  // Q, 16 x 128, two 64-column blocks
+  static constexpr int OFF_P = OFF_Q + 2 * QBLK;          // P[2 buffers], 16 x 128 keys each
+  static constexpr int OFF_XCH = OFF_P + 2 * 2 * QBLK;    // [2][4 warps][16] fp32
+  static constexpr int OFF_BAR = OFF_XCH + 2 * 4 * NQP * 4;
+  static constexpr int B_FULL = 0, B_EMPTY = NST, B_SFULL = 2 * NST, B_PFULL = B_SFULL + 2,
+                       B_PVDONE = B_PFULL + 2, B_XCH = B_PVDONE + 2, B_QREADY = B_XCH + 1, B_DRAIN = B_QREADY + 1,
+                       NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem slot, abort flag
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;
+  static constexpr int NUM_THREADS = 6 * 32;
+  static constexpr uint32_t TMEM_COLS = 64;               // Sᵀ[2] at 0, 16; Oᵀ_tile[2] at 32, 48
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int NQ>
+__global__ void __launch_bounds__(DecMmaCfg::NUM_THREADS, 1)
+    fa_decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const DecodeParams p) {
+  using C = DecMmaCfg;
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_base + pad;
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = p.B * p.H * p.splits;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::B_FULL + s), 1);
+      mbar_init(bar(C::B_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_SFULL + b), 1);
+      mbar_init(bar(C::B_PFULL + b), 128);
+      mbar_init(bar(C::B_PVDONE + b), 1);
+    }
+    mbar_init(bar(C::B_XCH), 128);
+    mbar_init(bar(C::B_QREADY), 128);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp < 4) {  // P rows past Nq stay zero for good (finite B operand)
+    for (int i = threadIdx.x; i < 2 * 2 * C::QBLK / 16; i += 128)
+      reinterpret_cast<uint4*>(smem + C::OFF_P)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int t = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int bh = item / p.splits, split = item - (item / p.splits) * p.splits;
+        const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+        const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
+        for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
+          const int st = t % C::NST;
+          if (t >= C::NST && !wait_bounded(bar(C::B_EMPTY + st), ((t / C::NST) - 1) & 1, abort_flag, p.err,
+                                           p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+          for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(sb + C::OFF_K + st * C::TILE_BYTES + kb * C::BLK_BYTES, &tmK, bar(C::B_FULL + st),
+                        kb * 64, h, kt, b);
+            tma_load_4d(sb + C::OFF_V + st * C::TILE_BYTES + kb * C::BLK_BYTES, &tmV, bar(C::B_FULL + st),
+                        kb * 64, h, kt, b);
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < C::NST && s < t; ++s) {
+          const int last = s + ((t - 1 - s) / C::NST) * C::NST;
+          wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, C::NQP, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(D, C::NQP, true, false);
+      const uint64_t dK0 = sdesc_sw128(sb + C::OFF_K, 16, 1024);          // K tile, K-major
+      const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, C::BLK_BYTES, 1024);  // V tile as the MN-major A of Vᵀ
+      const uint64_t dQ = sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+      const uint64_t dP0 = sdesc_sw128(sb + C::OFF_P, 16, 1024);
+      int t = 0, n_item = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++n_item) {
+        const int split = item - (item / p.splits) * p.splits;
+        const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
+        if (!wait_bounded(bar(C::B_QREADY), n_item & 1, abort_flag, p.err, p.timeout_ns)) break;
+        for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
+          const int st = t % C::NST, bf = t & 1;
+          if (!wait_bounded(bar(C::B_FULL + st), (t / C::NST) & 1, abort_flag, p.err, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dK = sdesc_add(dK0, st * C::TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32, qoff = (kk / 4) * C::QBLK + (kk % 4) * 32;
+            mma_ss(tmem + 16 * bf, sdesc_add(dK, koff), sdesc_add(dQ, qoff), idesc_s, kk > 0);
+          }
+          tc_commit(bar(C::B_SFULL + bf));
+          if (!wait_bounded(bar(C::B_PFULL + bf), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dV = sdesc_add(dV0, st * C::TILE_BYTES), dP = sdesc_add(dP0, bf * 2 * C::QBLK);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tmem + 32 + 16 * bf, sdesc_add(dV, kk * 2048), sdesc_add(dP, (kk / 4) * C::QBLK + (kk % 4) * 32),
+                   idesc_o, kk > 0);
+          tc_commit(bar(C::B_PVDONE + bf));
+          tc_commit(bar(C::B_EMPTY + st));
+        }
+      }
+      tc_commit(bar(C::B_DRAIN));
+      wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax, P, running O
+    const float c = p.scale_log2;
+    const int r = warp * 32 + lane;  // TMEM lane: key of the tile (Sᵀ, P), head dimension (Oᵀ)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+    int t = 0, nx = 0, n_item = 0;
+    bool ok = true;
+    // One exchange of a value per query among the four warps: warp maxima or
+    // sums in, the four per query out (mbarrier with a bounded wait).
+    auto exchange = [&](float (&v)[NQ], float (&out)[4][NQ]) -> bool {
+      float* slot = xch + (nx & 1) * 4 * C::NQP;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (lane == q) slot[warp * C::NQP + q] = v[q];
+      mbar_arrive(bar(C::B_XCH));
+      const bool got = wait_bounded(bar(C::B_XCH), nx & 1, abort_flag, p.err, p.timeout_ns);
+      ++nx;
+      if (!got) return false;
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) out[w][q] = slot[w * C::NQP + q];
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++n_item) {
+      const int bh = item / p.splits, split = item - (item / p.splits) * p.splits;
+      const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+      const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
+      // Q of this item into the 128-byte swizzled B layout (rows past Nq zero);
+      // every MMA that read the previous item's Q has completed (its Sᵀ was waited for).
+      for (int i = r; i < C::NQP * 16; i += 128) {
+        const int row = i / 16, c16 = i % 16;  // 16-byte chunk along d
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < p.Nq)
+          v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.Nq + row) * p.H + h) * D + c16 * 8);
+        *reinterpret_cast<uint4*>(smem + C::OFF_Q + (c16 / 8) * C::QBLK + row * 128 + (((c16 % 8) ^ (row & 7)) * 16)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_QREADY));
+      float m[NQ], lsum[NQ], ov[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        m[q] = -CUDART_INF_F;
+        lsum[q] = 0.f;
+        ov[q] = 0.f;
+      }
+      for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
+        const int bf = t & 1;
+        if (!wait_bounded(bar(C::B_SFULL + bf), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[16];
+        tmem_ld16(lane_addr + 16 * bf, sv);
+        tmem_wait_ld();
+        reg_fence(sv);
+        const int key = kt + r;
+        float x[NQ], wm[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const int lim = p.causal ? p.Nk - p.Nq + q : p.Nk - 1;  // last key query q sees
+          x[q] = (q < p.Nq && key <= lim && key < p.Nk) ? __uint_as_float(sv[q]) * c : -CUDART_INF_F;
+          wm[q] = x[q];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) wm[q] = fmaxf(wm[q], __shfl_xor_sync(0xffffffffu, wm[q], off));
+        }
+        float all[4][NQ];
+        if (!exchange(wm, all)) {
+          ok = false;
+          break;
+        }
+        float alpha[NQ];
+        const uint32_t prow = C::OFF_P + bf * 2 * C::QBLK + (r / 64) * C::QBLK;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const float m_new = fmaxf(fmaxf(m[q], fmaxf(all[0][q], all[1][q])), fmaxf(all[2][q], all[3][q]));
+          alpha[q] = (m[q] == -CUDART_INF_F) ? 0.f : ex2_approx(m[q] - m_new);
+          const float pq = (x[q] == -CUDART_INF_F) ? 0.f : ex2_approx(x[q] - m_new);
+          lsum[q] = fmaf(lsum[q], alpha[q], pq);
+          m[q] = m_new;
+          // P[q][key r]: row q of the K-major B operand, keys contiguous
+          const uint32_t byte = (r % 64) * 2;
+          const uint16_t pb = static_cast<uint16_t>(pack_bf16x2(pq, 0.f));
+          *reinterpret_cast<uint16_t*>(smem + prow + q * 128 + ((((byte >> 4) ^ (q & 7)) << 4) | (byte & 15))) = pb;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::B_PFULL + bf));
+        if (!wait_bounded(bar(C::B_PVDONE + bf), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t ot[16];
+        tmem_ld16(lane_addr + 32 + 16 * bf, ot);
+        tmem_wait_ld();
+        reg_fence(ot);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) ov[q] = fmaf(ov[q], alpha[q], __uint_as_float(ot[q]));
+      }
+      if (!ok) break;
+      // ---- the item's partial per query: l summed over the 128 keys' threads
+      float ws[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        ws[q] = lsum[q];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ws[q] += __shfl_xor_sync(0xffffffffu, ws[q], off);
+      }
+      float all[4][NQ];
+      if (!exchange(ws, all)) break;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q >= p.Nq) break;
+        const size_t idx = static_cast<size_t>(item) * p.Nq + q;
+        p.o_part[idx * D + r] = ov[q];
+        if (r == 0) {
+          p.ml_part[idx * 2 + 0] = m[q];
+          p.ml_part[idx * 2 + 1] = (all[0][q] + all[1][q]) + (all[2][q] + all[3][q]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // One warp per (sequence, head, query): O = Σ 2^(m_p − m) O_p / Σ 2^(m_p − m) l_p
 // over the splits partials of the head, m = max m_p; LSE = ln 2 · (m + log2 l).
 // The partials' weights are formed 32 at a time, one per lane, and the O
@@ -417,9 +717,33 @@ cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const
   return cudaGetLastError();
 }
 
+template <int NQ>
+cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                              cudaStream_t s) {
+  using C = DecMmaCfg;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_mma_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fa_decode_mma_kernel<NQ><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
+  fa_decode_merge_kernel<C::D><<<static_cast<unsigned>((warps * 32 + 63) / 64), 64, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                             cudaStream_t s) {
+  if (D == 128 && p.Nq >= 2) {  // several new tokens: the tensor-core kernel
+    if (p.Nq <= 2) return launch_decode_mma<2>(tk, tv, p, grid, s);
+    if (p.Nq <= 4) return launch_decode_mma<4>(tk, tv, p, grid, s);
+    return launch_decode_mma<8>(tk, tv, p, grid, s);
+  }
   if (p.Nq <= 1) return launch_decode_dq<D, 1>(tk, tv, p, grid, s);
   if (p.Nq <= 2) return launch_decode_dq<D, 2>(tk, tv, p, grid, s);
   if (p.Nq <= 4) return launch_decode_dq<D, 4>(tk, tv, p, grid, s);

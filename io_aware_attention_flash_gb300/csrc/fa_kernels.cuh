@@ -57,8 +57,8 @@ struct DecodeParams {
   const uint16_t* q;      // bf16 [B, Nq, H, d]
   uint16_t* o;            // bf16 [B, Nq, H, d]
   float* lse;             // fp32 [B, H, Nq]
-  float* o_part;          // fp32 [B·H·splits·4, Nq, d]: unnormalised partial outputs
-  float* ml_part;         // fp32 [B·H·splits·4, Nq, 2]: (max, sum) of each partial, base 2
+  float* o_part;          // fp32 [B·H·splits, Nq, d]: unnormalised partial outputs
+  float* ml_part;         // fp32 [B·H·splits, Nq, 2]: (max, sum) of each partial, base 2
   int B, H, Nq, Nk;
   int splits;             // key/value splits per (sequence, head)
   int split_len;          // keys per split, a multiple of 128
