@@ -461,26 +461,37 @@ __global__ void __launch_bounds__(DecMmaCfg::NUM_THREADS, 1)
       const uint64_t dV0 = sdesc_sw128(sb + C::OFF_V, C::BLK_BYTES, 1024);  // V tile as the MN-major A of Vᵀ
       const uint64_t dQ = sdesc_sw128(sb + C::OFF_Q, 16, 1024);
       const uint64_t dP0 = sdesc_sw128(sb + C::OFF_P, 16, 1024);
+      // Sᵀ of tile u (K from ring slot u mod 3, into TMEM buffer u mod 2).
+      auto issue_s = [&](int u) -> bool {
+        const int st = u % C::NST, bf = u & 1;
+        if (!wait_bounded(bar(C::B_FULL + st), (u / C::NST) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint64_t dK = sdesc_add(dK0, st * C::TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32, qoff = (kk / 4) * C::QBLK + (kk % 4) * 32;
+          mma_ss(tmem + 16 * bf, sdesc_add(dK, koff), sdesc_add(dQ, qoff), idesc_s, kk > 0);
+        }
+        tc_commit(bar(C::B_SFULL + bf));
+        return true;
+      };
       int t = 0, n_item = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++n_item) {
         const int split = item - (item / p.splits) * p.splits;
         const int k_lo = split * p.split_len, k_hi = min(p.Nk, k_lo + p.split_len);
         if (!wait_bounded(bar(C::B_QREADY), n_item & 1, abort_flag, p.err, p.timeout_ns)) break;
+        // Within an item Sᵀ of the next tile is issued before this tile's P is
+        // awaited (its TMEM buffer was read before the previous P arrived);
+        // across items it cannot be, as the next item's Q is staged only
+        // after this item's last output has been taken.
+        if (!issue_s(t)) break;
         for (int kt = k_lo; kt < k_hi; kt += kTile, ++t) {
           const int st = t % C::NST, bf = t & 1;
-          if (!wait_bounded(bar(C::B_FULL + st), (t / C::NST) & 1, abort_flag, p.err, p.timeout_ns)) {
+          if (kt + kTile < k_hi && !issue_s(t + 1)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t dK = sdesc_add(dK0, st * C::TILE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32, qoff = (kk / 4) * C::QBLK + (kk % 4) * 32;
-            mma_ss(tmem + 16 * bf, sdesc_add(dK, koff), sdesc_add(dQ, qoff), idesc_s, kk > 0);
-          }
-          tc_commit(bar(C::B_SFULL + bf));
           if (!wait_bounded(bar(C::B_PFULL + bf), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
