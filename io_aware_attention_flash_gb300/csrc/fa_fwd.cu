@@ -20,11 +20,11 @@
 // Online softmax ("LLM Systems 22", section 3.1; "08 · FlashAttention",
 // section 二) with the scale folded into the base-2 exponent
 // (c = scale·log2 e) and the output kept unnormalised until the end.  The
-// reference max m_ref is only moved when the tile max exceeds it by more than
-// 2^8 in exponent terms; otherwise P may exceed 1 (by at most 256) and the
-// rescale of O in TMEM is skipped ("LLM Systems 22", section 4.2.1: an online
-// softmax variant that skips most rescaling).  The result is exact after the
-// final division by l.
+// reference max m_ref is the first key tile's row max and is only moved when
+// a later tile's row sum reaches 2^40 (P may exceed 1, by less than 2^40);
+// otherwise neither a max pass nor a rescale of O in TMEM runs ("LLM Systems
+// 22", section 4.2.1: an online softmax variant that skips most rescaling).
+// The result is exact after the final division by l.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -320,67 +320,77 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
         }
         // Row max: three-input max into 4 independent partial maxima (a single
         // running max is a long dependency chain).
-        float mx[4];
+        auto row_max = [&]() -> float {
+          float mx[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = -CUDART_INF_F;
+          for (int k = 0; k < 4; ++k) mx[k] = -CUDART_INF_F;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+          for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(s[ch][2 * i]), __uint_as_float(s[ch][2 * i + 1]));
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-
-        if (j == 0) {
-          m_ref = mt;
-        } else {
-          const bool need = (mt - m_ref) * c > 8.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2_approx((m_ref - mt) * c) : 1.0f;
-            if (need) {
-              m_ref = mt;
-              l *= alpha;
-            }
-            // 16 columns at a time: the 128 S values of the row stay live here.
-#pragma unroll 1
-            for (int ch = 0; ch < D / 16; ++ch) {
-              uint32_t o[16];
-              tmem_ld16(tO + ch * 16, o);
-              tmem_wait_ld();
-              reg_fence(o);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(tO + ch * 16, o);
-            }
-            tmem_wait_st();
-          }
-        }
-        const float mc = (m_ref == -CUDART_INF_F) ? 0.f : m_ref * c;
+            for (int i = 0; i < 16; ++i)
+              mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(s[ch][2 * i]), __uint_as_float(s[ch][2 * i + 1]));
+          return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        };
+        // P = 2^(c·s − c·m_ref) as bf16 over S; returns the tile's row sum.
         // Column pairs go through the paired fp32 instructions: c·s − c·m for
         // two columns per FMA, and 4 paired partial row sums (the same 8
         // partial sums, in the same order, as one sum per column mod 8).
-        const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
-        uint64_t ls2[4];
+        auto p_pass = [&]() -> float {
+          const float mc = (m_ref == -CUDART_INF_F) ? 0.f : m_ref * c;
+          const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+          uint64_t ls2[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
+          for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(s[ch][2 * e]), __uint_as_float(s[ch][2 * e + 1])), c2, nmc2), x0,
-                      x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            ls2[e & 3] = fadd2(ls2[e & 3], f2_pack(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(__uint_as_float(s[ch][2 * e]), __uint_as_float(s[ch][2 * e + 1])), c2, nmc2),
+                        x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              ls2[e & 3] = fadd2(ls2[e & 3], f2_pack(p0, p1));
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + ch * 16, pk);
           }
-          tmem_st16(tS + ch * 16, pk);
-        }
-        float ls[8];
+          float ls[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) f2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+          for (int k = 0; k < 4; ++k) f2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
+          return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        };
+        // The reference m_ref is the first key tile's row max.  Later tiles are
+        // exponentiated against it without a max pass: the reference only has
+        // to be common to the row, and the result is exact after the final
+        // division by l ("LLM Systems 22", section 4.2.1: rescaling only when
+        // needed).  A tile whose row sum leaves [0, 2^40) (a score far above
+        // the reference, or a non-finite sum) takes its exact max, moves the
+        // reference up, rescales O and l, and is exponentiated again: P stays
+        // below 2^40 and O in fp32 range.
+        if (j == 0) m_ref = row_max();
+        float lt = p_pass();
+        if (__any_sync(0xffffffffu, !(lt < 0x1p40f))) {
+          const float m_new = fmaxf(m_ref, row_max());
+          const float alpha = (m_ref == -CUDART_INF_F) ? 0.f : ex2_approx((m_ref - m_new) * c);
+          m_ref = m_new;
+          l *= alpha;
+          // 16 columns at a time: the 128 S values of the row stay live here.
+#pragma unroll 1
+          for (int ch = 0; ch < D / 16; ++ch) {
+            uint32_t o[16];
+            tmem_ld16(tO + ch * 16, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + ch * 16, o);
+          }
+          tmem_wait_st();
+          lt = p_pass();
+        }
+        l += lt;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + t));

@@ -107,3 +107,27 @@ def test_nondefault_stream_and_scale():
     O, L = oracle.forward(f64(q), f64(k), f64(v), 0.3, True)
     assert np.abs(f64(o) - O).max() <= O_ATOL
     assert np.abs(f64(lse) - L).max() <= LSE_ATOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_scores_growing_along_the_keys(d, causal):
+    """Scores that grow by far more than 2^40 (in base-2 exponent terms)
+    across the key tiles: the first tile's row max is a poor reference, so
+    the kernel must move it (rescaling O and l) on later tiles.  Also a
+    single late key far above everything before it."""
+    fa = require_gpu()
+    B, N, H = 1, 700, 2
+    g = torch.Generator().manual_seed(17)
+    ramp = torch.arange(N, dtype=torch.float32) / N
+    q = torch.full((B, N, H, d), 1.0)
+    k = (ramp[None, :, None, None] * 6.0).expand(B, N, H, d).clone()
+    k[:, 450, 1] = 9.0   # head 1: one key far above its neighbours
+    v = torch.randn(B, N, H, d, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o, lse = fa.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal)
+    torch.cuda.synchronize()
+    assert_no_device_error(fa)
+    O, L = oracle.forward(f64(q), f64(k), f64(v), d ** -0.5, causal)
+    assert np.abs(f64(o) - O).max() <= O_ATOL
+    assert np.abs(f64(lse) - L).max() <= LSE_ATOL
