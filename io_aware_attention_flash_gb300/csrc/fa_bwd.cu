@@ -498,12 +498,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[16];
+        // Two copies of the loop: the test of the mask would otherwise cost a
+        // compare and a select per element on every tile, not only on the
+        // diagonal one and past the sequence end.
+        if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = 64 * g + 32 * ch + e;
-          float pe = ex2_approx(fmaf(__uint_as_float(pr[ch][e]), c, -lse2[col]));
-          if (need_mask && (row_dead || q0 + col < kv_row)) pe = 0.f;
-          pr[ch][e] = __float_as_uint(pe);
+          for (int e = 0; e < 32; ++e) {
+            const int col = 64 * g + 32 * ch + e;
+            float pe = ex2_approx(fmaf(__uint_as_float(pr[ch][e]), c, -lse2[col]));
+            if (row_dead || q0 + col < kv_row) pe = 0.f;
+            pr[ch][e] = __float_as_uint(pe);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = 64 * g + 32 * ch + e;
+            pr[ch][e] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(pr[ch][e]), c, -lse2[col])));
+          }
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e)
