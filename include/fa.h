@@ -235,6 +235,9 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *              from ex2.approx over [-30, 8]; -1 if a clamped input gave a
  *              negative, NaN or non-tiny value
  *          43: step 40 with a quarter of the pairs through the polynomial exp2
+ *          44, 45: SM cycles for the forward softmax on one 128 x 128 score
+ *              tile in TMEM with no MMA running, one tile (four warps, 44)
+ *              or two tiles at once (eight warps, 45)
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

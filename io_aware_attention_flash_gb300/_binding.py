@@ -67,7 +67,8 @@ MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk"
               "sync_cycles_timer_queue_full": 37,
               "softmax_ex2_cvt_per_sm_clk": 38, "softmax_ex2_intpack_per_sm_clk": 39,
               "softmax_step_per_sm_clk": 40, "softmax_step_intpack_per_sm_clk": 41,
-              "ex2_poly_max_rel_err": 42, "softmax_step_quarter_poly_per_sm_clk": 43}
+              "ex2_poly_max_rel_err": 42, "softmax_step_quarter_poly_per_sm_clk": 43,
+              "softmax_tile_cycles_1tile": 44, "softmax_tile_cycles_2tiles": 45}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

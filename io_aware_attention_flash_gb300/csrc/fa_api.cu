@@ -509,7 +509,7 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
   if (!result) return FA_ERR_NULL;
-  if (which < 0 || which > 43 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  if (which < 0 || which > 45 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
   FA_TRY(check_arch());
   if (which >= 12 && which <= 16) {
     // Reduce-add throughput into a 64 MiB fp32 array shaped [8192, 16, 128].

@@ -95,6 +95,94 @@ __device__ __forceinline__ uint32_t random_bf16x2(uint32_t i) {
   return lo | (hi << 16);
 }
 
+// The forward kernel's softmax on one 128 x 128 score tile, alone: no MMA
+// runs.  Warpgroup t (t < NWG) reads S_t (128 columns of TMEM, random fp32
+// scores), takes the row max, forms P = 2^(c·s − c·m) with the paired FMA,
+// ex2, the paired row-sum adds and the bf16 packing, and stores P (64
+// columns) into a separate TMEM region, as the kernel does, `iters` times.
+// Cycles per tile show whether the softmax's instruction stream or its
+// surroundings in the kernel set its duration.
+template <int NWG>
+__global__ void __launch_bounds__(320, 1) softmax_tile_kernel(int iters, unsigned long long* cycles, float* sink) {
+  // (register budget of the forward kernel's 320 threads)
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int t = warp / 4, wq = warp % 4;
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t tS = lane_addr + 128 * t, tP = lane_addr + 256 + 64 * t;
+  {
+    uint32_t z[32];
+    for (int cc = 0; cc < 128; cc += 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = __float_as_uint(-4.0f + 8.0f * ((random_bf16x2(threadIdx.x * 131 + cc + i) & 0xFFFFu) / 65536.0f));
+      tmem_st32(tS + cc, z);
+    }
+    tmem_wait_st();
+  }
+  __syncthreads();
+  const float c = 0.1275f;
+  float l = 0.f;
+  const unsigned long long t0 = clock64();
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+    uint32_t s[4][32];
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) tmem_ld32(tS + ch * 32, s[ch]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) reg_fence(s[ch]);
+    float mx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mx[k] = -CUDART_INF_F;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(s[ch][2 * i]), __uint_as_float(s[ch][2 * i + 1]));
+    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    const float mc = mt * c;
+    const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+    uint64_t ls2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float x0, x1;
+        f2_unpack(ffma2(f2_pack(__uint_as_float(s[ch][2 * e]), __uint_as_float(s[ch][2 * e + 1])), c2, nmc2), x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        ls2[e & 3] = fadd2(ls2[e & 3], f2_pack(p0, p1));
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(tP + ch * 16, pk);
+    }
+    float ls[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
+    l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+    tmem_wait_st();
+  }
+  const unsigned long long t1 = clock64();
+  if (l == 12345.f) sink[threadIdx.x % kMaxSms] = l;
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // Accuracy of ex2_poly2 against ex2.approx.ftz.f32 over x in [-30, 8]
 // (2^20 points): the largest relative difference, as fp32 bits in *out (a
 // positive float orders as its bits).  Inputs far below the clamp (-1e4,
@@ -576,6 +664,8 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
     case 40: unit_rate_kernel<5><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 41: unit_rate_kernel<6><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
     case 43: unit_rate_kernel<7><<<sms, threads, 0, s>>>(iters, cyc, sink); break;
+    case 44: softmax_tile_kernel<1><<<sms, 128, 0, s>>>(iters, cyc, sink); break;
+    case 45: softmax_tile_kernel<2><<<sms, 256, 0, s>>>(iters, cyc, sink); break;
     case 42: {  // accuracy, not a rate
       unsigned int* acc = reinterpret_cast<unsigned int*>(cyc);
       if ((e = cudaMemsetAsync(acc, 0, 2 * sizeof(unsigned int), s)) != cudaSuccess) return e;
@@ -637,7 +727,7 @@ cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, 
   if ((e = cudaMemcpy(host_cyc, cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return e;
   double acc = 0;
-  if (which >= 25 && which <= 37) {  // cycles per step, averaged over the SMs
+  if ((which >= 25 && which <= 37) || which == 44 || which == 45) {  // cycles per step, averaged over the SMs
     for (int i = 0; i < sms; ++i) acc += static_cast<double>(host_cyc[i]) / iters;
     *result = acc / sms;
     return cudaSuccess;

@@ -18,6 +18,8 @@ pytestmark = gpu
     ("softmax_step_intpack_per_sm_clk", 4, 256),
     ("softmax_step_quarter_poly_per_sm_clk", 4, 256),
     ("ex2_poly_max_rel_err", 0, 1e-4),
+    ("softmax_tile_cycles_1tile", 50, 20000),
+    ("softmax_tile_cycles_2tiles", 50, 20000),
     ("mma_bf16_flop_per_sm_clk_n256", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128", 1024, 32768),
     ("mma_bf16_flop_per_sm_clk_n128_tmem_a", 1024, 32768),
