@@ -211,17 +211,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 
   // TMA issue of query tile ii's Q and dO into ring slot ii % NSQ (producer
   // thread).
-  auto load_qdo = [&](int ii) {
+  auto load_q = [&](int ii) {
     const int qs = ii % C::NSQ;
     const int qrow = sp.tma_row0 + (i_first + ii) * kTile;
     mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE_BYTES);
     for (int kb = 0; kb < C::KB; ++kb)
       tma_load_4d(sb + C::OFF_Q + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_QFULL + qs), kb * 64, sp.h,
                   qrow, sp.tma_b);
+  };
+  auto load_do = [&](int ii) {
+    const int qs = ii % C::NSQ;
+    const int qrow = sp.tma_row0 + (i_first + ii) * kTile;
     mbar_arrive_expect_tx(bar(C::B_DOFULL + qs), C::TILE_BYTES);
     for (int kb = 0; kb < C::KB; ++kb)
       tma_load_4d(sb + C::OFF_DO + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmdO, bar(C::B_DOFULL + qs), kb * 64,
                   sp.h, qrow, sp.tma_b);
+  };
+  auto load_qdo = [&](int ii) {
+    load_q(ii);
+    load_do(ii);
   };
   // K, V and the query tiles whose ring slots start empty are loaded by the
   // producer as soon as it has initialised the barriers, so the first loads
@@ -277,28 +285,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
       // The dQ of query tile t is staged (fp32, 128-byte swizzled, one 4 KB
-      // slice per 32 rows and 32 columns) over Q_t and dO_t in ring slot
-      // t % NSQ once the MMAs have consumed them.  This thread adds
-      // the slices into the accumulator with TMA bulk reduce-adds and reuses
-      // the slot for tile t + NSQ once the reduces have read it.
-      auto reduce_tile = [&](int t) -> bool {
+      // slice per 32 rows and 32 columns: columns 0-63 over Q_t, 64-127 over
+      // dO_t) in ring slot t % NSQ once the MMAs have consumed them.  This
+      // thread adds the slices into the accumulator with TMA bulk reduce-adds
+      // and reuses the slot for tile t + NSQ once the reduces have read it.
+      // The reduces read at the L2's reduce rate, so a slot takes thousands of
+      // cycles to empty: the half over Q_t goes first, in its own bulk group,
+      // and Q_{t+NSQ} (needed first, for Sᵀ) is loaded as soon as that half
+      // has been read, dO_{t+NSQ} after the other half.
+      auto reduce_half = [&](int t, int half) {
         const int qs = t % C::NSQ;
-        if (!wait_bounded(bar(C::B_STAGED + qs), (t / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) return false;
         const int q0 = (i_first + t) * kTile;
 #pragma unroll 1
         for (int wq = 0; wq < 4; ++wq) {
 #pragma unroll
-          for (int c = 0; c < C::NCHT; ++c)
+          for (int c = half * (C::NCHT / 2); c < (half + 1) * (C::NCHT / 2); ++c)
             tma_reduce_add_3d(&tmDQ, sb + C::dq_slot(qs, c, wq), 32 * c, sp.h, sp.row_base + q0 + 32 * wq);
         }
         bulk_commit_group();
+      };
+      auto reduce_tile = [&](int t) -> bool {
+        const int qs = t % C::NSQ;
+        if (!wait_bounded(bar(C::B_STAGED + qs), (t / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+        reduce_half(t, 0);
+        reduce_half(t, 1);
         return true;
       };
       int fills = preloaded;
       for (int ii = preloaded; ii < nq; ++ii) {
         if (!reduce_tile(ii - C::NSQ)) break;
-        bulk_wait_group_read0();   // the slot's staged dQ has been read
-        load_qdo(ii);
+        bulk_wait_group_read<1>();  // the half over Q has been read
+        load_q(ii);
+        bulk_wait_group_read0();    // and the half over dO
+        load_do(ii);
         ++fills;
       }
       if (!*abort_flag) {
