@@ -15,6 +15,9 @@ pytestmark = gpu
 SHAPES = [
     (1, 1, 1, 1, 128), (2, 3, 1, 100, 64), (1, 2, 2, 129, 128), (1, 2, 4, 1000, 128), (2, 2, 3, 4097, 128),
     (1, 4, 8, 700, 64), (3, 2, 5, 2500, 128), (1, 3, 8, 9000, 128), (2, 2, 6, 6, 64),
+    # the tensor-core kernel (d = 128, 2..8 tokens) on a cache shorter than
+    # one key tile, and on 7 tokens (padded to 8, then to the MMA's 16)
+    (2, 2, 6, 6, 128), (1, 2, 7, 383, 128), (1, 1, 2, 2, 128), (3, 1, 4, 64, 64),
 ]
 
 
