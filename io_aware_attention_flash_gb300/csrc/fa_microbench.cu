@@ -106,7 +106,7 @@ template <int NWG>
 __global__ void __launch_bounds__(320, 1) softmax_tile_kernel(int iters, unsigned long long* cycles, float* sink) {
   // (register budget of the forward kernel's 320 threads)
   __shared__ uint32_t tmem_slot;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   if (warp == 0) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
