@@ -271,9 +271,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
         tc_commit(bar(C::B_VEMPTY + vs));
         if (next) tc_commit(bar(C::B_KEMPTY + ks1));
       }
-      // O_t is final.  (Committing each tile's barrier inside the loop, right
-      // after its last PV, measured slower: this thread's instruction stream
-      // is the loop's limiter.)
+      // O_t is final.  (Committing a tile's barrier inside the loop, right
+      // after its last PV, so that its epilogue overlaps the other tile's last
+      // iteration, measured no faster.)
       if (ok)
         for (int t = 0; t < NQT; ++t) tc_commit(bar(C::B_ODONE + t));
       // Every MMA issued so far must finish before TMEM is released.
