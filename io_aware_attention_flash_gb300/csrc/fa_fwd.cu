@@ -36,14 +36,20 @@
 namespace fa {
 namespace {
 
-template <int D>
+// NQT_ query tiles per CTA: two at d = 128 (one CTA per SM, the two tiles'
+// MMAs and softmaxes interleaved); one at d = 64, where a CTA's tensor memory
+// (256 columns) and shared memory (~97 KB) let two CTAs share an SM, so one
+// CTA's MMAs fill the tensor pipe while the other's softmax runs, and one
+// CTA's prologue and epilogue overlap the other's work.
+template <int D, int NQT_>
 struct FwdCfg {
-  static constexpr int NQT = 2;                         // query tiles per CTA
+  static constexpr int NQT = NQT_;                      // query tiles per CTA
+  static constexpr int MIN_BLOCKS = NQT == 1 ? 2 : 1;   // CTAs per SM
   static constexpr int KB = D / 64;                     // 128-byte swizzle blocks per row
   static constexpr int BLK_BYTES = kTile * 128;         // one 128-row x 64-col block
   static constexpr int TILE_BYTES = KB * BLK_BYTES;     // one 128 x D tile
-  static constexpr int NSK = (D == 128) ? 3 : 4;        // K ring depth
-  static constexpr int NSV = (D == 128) ? 2 : 4;        // V ring depth
+  static constexpr int NSK = (D == 128 || NQT == 1) ? 3 : 4;  // K ring depth
+  static constexpr int NSV = (D == 128 || NQT == 1) ? 2 : 4;  // V ring depth
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQT * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
@@ -68,19 +74,22 @@ struct FwdCfg {
   static constexpr int NUM_THREADS = NUM_WARPS * 32;
   static constexpr int PRODUCER_WARP = 4 * NQT;
   static constexpr int MMA_WARP = 4 * NQT + 1;
-  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_COLS = NQT == 2 ? 512 : 256;
   // TMEM columns: S_t (P_t aliases its first 64 columns) and O_t.
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return t * 128; }
-  __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256 + t * D; }
+  __host__ __device__ static constexpr uint32_t O_COL(int t) { return NQT * 128 + t * D; }
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(NQT * (128 + D) <= static_cast<int>(TMEM_COLS), "tensor memory budget");
+  // CTAs sharing an SM: 228 KB of shared memory, 1 KB of it reserved per CTA.
+  static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 233472, "shared memory for the CTAs of one SM");
 };
 
-template <int D>
-__global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
+template <int D, int NQT_>
+__global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>::MIN_BLOCKS)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NQT_>;
   constexpr int NQT = C::NQT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -469,18 +478,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::NUM_THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, int NQT>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                          const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NQT>;
   static bool configured = false;  // per process; attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_fwd_kernel<D, NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(nseq * p.sv.H, (max_seqlen + kTile * C::NQT - 1) / (kTile * C::NQT));
-  fa_fwd_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, to, p);
+  fa_fwd_kernel<D, NQT><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -488,8 +498,8 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, p, nseq, max_seqlen, s);
-  return launch_fwd_d<128>(tq, tk, tv, to, p, nseq, max_seqlen, s);
+  if (d == 64) return launch_fwd_d<64, 1>(tq, tk, tv, to, p, nseq, max_seqlen, s);
+  return launch_fwd_d<128, 2>(tq, tk, tv, to, p, nseq, max_seqlen, s);
 }
 
 }  // namespace fa
