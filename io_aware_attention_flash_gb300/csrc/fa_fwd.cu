@@ -54,10 +54,10 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQT * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
-  // barriers: q, kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT], odone[NQT],
-  // ostaged[NQT], drain
-  static constexpr int B_Q = 0;
-  static constexpr int B_KFULL = 1;
+  // barriers: q[NQT], kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT],
+  // odone[NQT], ostaged[NQT], drain
+  static constexpr int B_Q = 0;                         // [NQT]: query tile t landed
+  static constexpr int B_KFULL = NQT;
   static constexpr int B_KEMPTY = B_KFULL + NSK;
   static constexpr int B_VFULL = B_KEMPTY + NSK;
   static constexpr int B_VEMPTY = B_VFULL + NSV;
@@ -118,17 +118,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
   }
 
   // TMA issue of Q and of K/V tile j into its ring slot (producer thread).
-  auto load_q = [&]() {
-    uint32_t qbytes = 0;
-    for (int t = 0; t < NQT; ++t)
-      if (nkv[t] > 0) qbytes += C::TILE_BYTES;
-    mbar_arrive_expect_tx(bar(C::B_Q), qbytes);
-    for (int t = 0; t < NQT; ++t) {
-      if (nkv[t] == 0) continue;
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_4d(sb + C::OFF_Q + t * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_Q), kb * 64, sp.h,
-                    sp.tma_row0 + q0 + t * kTile, sp.tma_b);
-    }
+  auto load_q = [&](int t) {
+    mbar_arrive_expect_tx(bar(C::B_Q + t), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_Q + t * C::TILE_BYTES + kb * C::BLK_BYTES, &tmQ, bar(C::B_Q + t), kb * 64, sp.h,
+                  sp.tma_row0 + q0 + t * kTile, sp.tma_b);
   };
   auto load_k = [&](int j) {
     const int ks = j % C::NSK;
@@ -150,7 +144,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
   const int preloaded = min(nkv_max, C::NSV);
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
-    mbar_init(bar(C::B_Q), 1);
+    for (int t = 0; t < NQT; ++t) mbar_init(bar(C::B_Q + t), 1);
     for (int s = 0; s < C::NSK; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
       mbar_init(bar(C::B_KEMPTY + s), 1);
@@ -172,8 +166,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    load_q();
-    for (int j = 0; j < preloaded; ++j) {
+    // In the order the first MMAs need them: Q_0 and K_0 (for S_0), then the
+    // other query tiles, then V_0, so S_0 of the first key tile can start
+    // before the whole set has landed.
+    load_q(0);
+    if (preloaded > 0) load_k(0);
+    for (int t = 1; t < NQT; ++t)
+      if (nkv[t] > 0) load_q(t);
+    if (preloaded > 0) load_v(0);
+    for (int j = 1; j < preloaded; ++j) {
       load_k(j);
       load_v(j);
     }
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
       }
       if (*abort_flag) {
         // Unwinding: let every copy already issued land before the CTA exits.
-        wait_drain(bar(C::B_Q), 0, p.err, p.timeout_ns);
+        for (int t = 0; t < NQT; ++t)
+          if (nkv[t] > 0) wait_drain(bar(C::B_Q + t), 0, p.err, p.timeout_ns);
         for (int s = 0; s < C::NSK && s < k_fills; ++s)
           wait_drain(bar(C::B_KFULL + s), ((s + ((k_fills - 1 - s) / C::NSK) * C::NSK) / C::NSK) & 1, p.err,
                      p.timeout_ns);
@@ -240,18 +242,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
           mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, sdesc_add(dV, kk * 2048), idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bounded(bar(C::B_Q), 0, abort_flag, p.err, p.timeout_ns) &&
-                wait_bounded(bar(C::B_KFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < NQT; ++t) {
-          if (nkv[t] > 0) {
-            issue_s(t, 0);
-            tc_commit(bar(C::B_SFULL + t));
-          }
+      bool ok = wait_bounded(bar(C::B_KFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
+      for (int t = 0; ok && t < NQT; ++t) {
+        if (nkv[t] > 0) {
+          ok = wait_bounded(bar(C::B_Q + t), 0, abort_flag, p.err, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t, 0);
+          tc_commit(bar(C::B_SFULL + t));
         }
-        tc_commit(bar(C::B_KEMPTY + 0));
       }
+      if (ok) tc_commit(bar(C::B_KEMPTY + 0));
       for (int j = 0; ok && j < nkv_max; ++j) {
         const int vs = j % C::NSV;
         const bool next = j + 1 < nkv_max;
