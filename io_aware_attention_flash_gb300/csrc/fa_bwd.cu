@@ -133,8 +133,9 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + NSQ * TILE_BYTES;      // dSᵀ, 128 key rows x 128 q, 2 blocks
   static constexpr int OFF_STAT = OFF_DS + 2 * BLK_BYTES;       // [2][2][128] fp32: log2e·LSE and D
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kTile * 4;
-  static constexpr int B_KV = 0;
-  static constexpr int B_QFULL = 1;
+  static constexpr int B_K = 0;
+  static constexpr int B_V = 1;
+  static constexpr int B_QFULL = 2;
   static constexpr int B_DOFULL = B_QFULL + NSQ;
   // B_STAGED[s]: the drain warps have staged the dQ of the query tile in
   // ring slot s over that tile's (consumed) Q and dO.
@@ -237,7 +238,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
   const int preloaded = min(nq, C::NSQ);
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
-    mbar_init(bar(C::B_KV), 1);
+    mbar_init(bar(C::B_K), 1);
+    mbar_init(bar(C::B_V), 1);
     for (int s = 0; s < C::NSQ; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1);
       mbar_init(bar(C::B_DOFULL + s), 1);
@@ -260,14 +262,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
-    mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE_BYTES);
-    for (int kb = 0; kb < C::KB; ++kb) {
-      tma_load_4d(sb + C::OFF_K + kb * C::BLK_BYTES, &tmK, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
-                  sp.tma_b);
-      tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_KV), kb * 64, sp.h, sp.tma_row0 + kv0,
-                  sp.tma_b);
-    }
-    for (int ii = 0; ii < preloaded; ++ii) load_qdo(ii);
+    // In the order the first MMAs need them: K and Q_0 (Sᵀ_0), then V and
+    // dO_0 (dPᵀ_0), then the rest of the ring.
+    mbar_arrive_expect_tx(bar(C::B_K), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_K + kb * C::BLK_BYTES, &tmK, bar(C::B_K), kb * 64, sp.h, sp.tma_row0 + kv0, sp.tma_b);
+    if (preloaded > 0) load_q(0);
+    mbar_arrive_expect_tx(bar(C::B_V), C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_V), kb * 64, sp.h, sp.tma_row0 + kv0, sp.tma_b);
+    if (preloaded > 0) load_do(0);
+    for (int ii = 1; ii < preloaded; ++ii) load_qdo(ii);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -326,7 +331,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       }
       bulk_wait_group_read0();   // every reduce has read its slot; the adds land before the grid ends
       if (*abort_flag) {
-        wait_drain(bar(C::B_KV), 0, p.err, p.timeout_ns);
+        wait_drain(bar(C::B_K), 0, p.err, p.timeout_ns);
+        wait_drain(bar(C::B_V), 0, p.err, p.timeout_ns);
         for (int s = 0; s < C::NSQ && s < fills; ++s) {
           const uint32_t ph = ((s + ((fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1;
           wait_drain(bar(C::B_QFULL + s), ph, p.err, p.timeout_ns);
@@ -357,13 +363,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
           mma_ss(dst, sdesc_add(a, koff), sdesc_add(b, koff), idesc_sp, kk > 0);
         }
       };
-      bool ok = wait_bounded(bar(C::B_KV), 0, abort_flag, p.err, p.timeout_ns) &&
+      bool ok = wait_bounded(bar(C::B_K), 0, abort_flag, p.err, p.timeout_ns) &&
                 wait_bounded(bar(C::B_QFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       if (ok) {
         tc_fence_after();
         issue_sp(region(0), kmK, kmQ);                                     // Sᵀ_0 -> R0
         tc_commit(bar(C::B_SFULL));
-        ok = wait_bounded(bar(C::B_DOFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
+        ok = wait_bounded(bar(C::B_V), 0, abort_flag, p.err, p.timeout_ns) &&
+             wait_bounded(bar(C::B_DOFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       }
       if (ok) {
         tc_fence_after();
