@@ -8,6 +8,8 @@ then fa_bwd (pre, main, post kernels).  Inputs are seeded synthetic bf16
 tensors already resident in device memory; L2 is flushed (a 256 MiB write)
 between timed steps, outside the per-step CUDA events.  FLOPs follow the
 usual convention: forward 4·B·H·N²·d, backward 2.5x, both halved when causal.
+The roofline's kernel (the backward main kernel) is timed in a second loop of
+K backward calls with CUDA events recorded right around it.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU with
 no collective on the data path (weak scaling); timing uses a barrier and the
@@ -239,19 +241,28 @@ def run_gpu(args, w):
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev_main = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize(dev)
+        # The K steps: nothing recorded between the backward's kernels, so each
+        # starts while its predecessor finishes (programmatic dependent launch).
         for i in range(K):
             flush.zero_()
             e = ev[i]
             e[0].record(stream)
             fa.fa_fwd(q, k, v, o, lse, w.causal)
             e[1].record(stream)
-            fa.fa_set_kernel_events(e[2], e[3])
             fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, wsp, w.causal)
-            e[4].record(stream)
+            e[2].record(stream)
+        # The backward main kernel alone (roofline): K more backward calls with
+        # events recorded right before and after it, which also keeps it apart
+        # from its neighbours.
+        for i in range(K):
+            flush.zero_()
+            fa.fa_set_kernel_events(ev_main[i][0], ev_main[i][1])
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, wsp, w.causal)
         torch.cuda.synchronize(dev)
         barrier()
         e2e = None
@@ -260,10 +271,10 @@ def run_gpu(args, w):
     if fa.fa_get_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
-    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
-    main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    main_ms = [e[0].elapsed_time(e[1]) for e in ev_main]
     t_step = statistics.mean(step_ms)
     t_step, t_fwd, t_bwd, t_main = max_over_ranks(
         [t_step, statistics.mean(fwd_ms), statistics.mean(bwd_ms), statistics.mean(main_ms)], dev)
@@ -290,7 +301,9 @@ def run_gpu(args, w):
                      "unit": "TFLOP/s", "frac": main_tflops / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 1.9 PFLOP/s bf16"},
-        "gpu_launches": 4 * K,
+        # 4 kernels per step (fwd; bwd pre, main, post), 3 per backward call
+        # of the main-kernel timing loop.
+        "gpu_launches": 7 * K,
         "clocks": clocks.summary(),
     }
     if not args.no_decode:

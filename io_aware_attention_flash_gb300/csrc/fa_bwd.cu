@@ -62,6 +62,7 @@ __device__ __forceinline__ void locate_row(const SeqView& sv, int nseq, int g, i
 // ----------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
+  grid_launch_dependents();  // the main kernel's prologue and first MMAs need nothing from here
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.sv.H;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
 // fa_bwd_post: dQ = bf16(scale · accumulator), 8 elements per thread.
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const BwdParams p, size_t n8) {
+  grid_dependency_wait();    // every reduce-add of the main kernel has landed
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const float4 a = reinterpret_cast<const float4*>(p.dq_accum)[2 * i];
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
+  grid_launch_dependents();  // the dQ conversion may be scheduled; it waits for this grid to finish
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
@@ -316,6 +319,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         reduce_half(t, 1);
         return true;
       };
+      // The first reduce-add needs the accumulator zeroed by the pre-pass
+      // (plain stores, possibly still running when this kernel started).
+      grid_dependency_wait();
+      fence_proxy_async_global();
       int fills = preloaded;
       for (int ii = preloaded; ii < nq; ++ii) {
         if (!reduce_tile(ii - C::NSQ)) break;
@@ -494,6 +501,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       buf[g * 128 + r] = v;
       mbar_arrive(bar(C::B_STAT + (ii & 1)));
     };
+    grid_dependency_wait();  // D comes from the pre-pass
     if (nq > 0) publish_stat(0, load_stat(0));
     float stat_next = nq > 1 ? load_stat(1) : 0.f;
     bool ok = true;
@@ -644,13 +652,17 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   dim3 grid(p.nseq * p.sv.H, (max_seqlen + kTile - 1) / kTile);
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
-  fa_bwd_main_kernel<D><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
-  e = cudaGetLastError();
+  // The main kernel starts while the pre-pass finishes, and the conversion
+  // while the main kernel's last CTAs run (each waits for its predecessor
+  // before reading what it wrote).  An event recorded between two kernels
+  // (timing the main kernel alone) keeps them apart.
+  e = launch_kernel(fa_bwd_main_kernel<D>, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, s, ev0 == nullptr, tq, tk, tv,
+                    tdo, tdq, p);
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(pairs) * D / 8;
-  fa_bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(p, n8);
-  return cudaGetLastError();
+  return launch_kernel(fa_bwd_post_kernel, dim3(static_cast<unsigned>((n8 + 255) / 256)), dim3(256), 0, s,
+                       ev1 == nullptr, p, n8);
 }
 
 }  // namespace

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
                            const DecodeParams p) {
   using C = DecCfg<D, QG>;
   static_assert(NQ % QG == 0, "queries split evenly over the query groups");
+  grid_launch_dependents();  // the merge may be scheduled; it waits for this grid to finish
   constexpr int NQW = NQ / QG;  // queries per compute warp
   constexpr int E = C::E;
   extern __shared__ uint8_t smem_raw[];
@@ -376,6 +377,7 @@ __global__ void __launch_bounds__(DecMmaCfg::NUM_THREADS, 1)
                          const DecodeParams p) {
   using C = DecMmaCfg;
   constexpr int D = C::D;
+  grid_launch_dependents();  // the merge may be scheduled; it waits for this grid to finish
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(DecMmaCfg::NUM_THREADS, 1)
 template <int D>
 __global__ void __launch_bounds__(64) fa_decode_merge_kernel(const DecodeParams p) {
   constexpr int E = D / 32;
+  grid_dependency_wait();  // the partials of the split kernel are complete
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= p.B * p.H * p.Nq) return;
@@ -724,8 +727,10 @@ cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
   // Two warps per block: the rows are few (B·H·Nq), so spread them over the SMs.
-  fa_decode_merge_kernel<D><<<static_cast<unsigned>((warps * 32 + 63) / 64), 64, 0, s>>>(p);
-  return cudaGetLastError();
+  // The merge is scheduled while the split kernel's last items run and
+  // waits for it before reading the partials.
+  return launch_kernel(fa_decode_merge_kernel<D>, dim3(static_cast<unsigned>((warps * 32 + 63) / 64)), dim3(64), 0, s,
+                       true, p);
 }
 
 template <int NQ>
@@ -743,8 +748,8 @@ cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, cons
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
-  fa_decode_merge_kernel<C::D><<<static_cast<unsigned>((warps * 32 + 63) / 64), 64, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(fa_decode_merge_kernel<C::D>, dim3(static_cast<unsigned>((warps * 32 + 63) / 64)), dim3(64), 0,
+                       s, true, p);
 }
 
 template <int D>
