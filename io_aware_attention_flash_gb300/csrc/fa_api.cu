@@ -153,8 +153,8 @@ thread_local cudaEvent_t t_main_end = nullptr;
 
 size_t pad256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
-// Shape limits: int32 row indices, the grid's x extent (sequences x heads) and
-// y extent (query or key tiles) within CUDA's limits.
+// Shape limits: int32 row indices, and one CTA per (sequence, head, tile)
+// within the one-dimensional grid's 2^31 - 1 blocks.
 fa_status check_common(int H, int d, float scale) {
   if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
   if (H <= 0 || H > 65535) return FA_ERR_SHAPE;
@@ -166,7 +166,7 @@ fa_status check_rows(long long nseq, long long rows, long long max_seqlen, int H
   if (nseq <= 0 || rows <= 0 || max_seqlen <= 0) return FA_ERR_SHAPE;
   if (rows > 0x7fffffffLL || nseq * H > 0x7fffffffLL) return FA_ERR_SHAPE;
   if (rows * H * static_cast<long long>(d) > (1LL << 40)) return FA_ERR_SHAPE;
-  if ((max_seqlen + fa::kTile - 1) / fa::kTile > 65535) return FA_ERR_SHAPE;
+  if (nseq * H * ((max_seqlen + fa::kTile - 1) / fa::kTile) > 0x7fffffffLL) return FA_ERR_SHAPE;
   return FA_OK;
 }
 

@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SeqPos sp = seq_pos(p.sv);
-  const int j = blockIdx.y;           // key tile; heavy (small j) tiles first under a causal mask
+  int pair, j;                        // j: key tile; heavy (small j) tiles first under a causal mask
+  cta_item(p.sv, pair, j);
+  if (pair >= p.sv.npairs) return;
+  const SeqPos sp = seq_pos(p.sv, pair);
   const int kv0 = j * kTile;
   if (kv0 >= sp.seqlen) return;
   const int nq_total = (sp.seqlen + kTile - 1) / kTile;
@@ -646,18 +648,27 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  int sms = 0;
+  cudaError_t e = current_sm_count(sms);
+  if (e != cudaSuccess) return e;
+  BwdParams pm = p;
+  pm.sv.npairs = p.nseq * p.sv.H;
+  pm.sv.ntiles = (max_seqlen + kTile - 1) / kTile;
+  pm.sv.pair_group = pair_group_size(pm.sv.npairs, pm.sv.ntiles, sms);  // one CTA per SM
+  const long long ctas = grid_ctas(pm.sv.npairs, pm.sv.ntiles, pm.sv.pair_group);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(ctas));
   const long long pairs = static_cast<long long>(p.rows) * p.sv.H;
   fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pairs * 32 + 255) / 256), 256, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(p.nseq * p.sv.H, (max_seqlen + kTile - 1) / kTile);
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
   // The main kernel starts while the pre-pass finishes, and the conversion
   // while the main kernel's last CTAs run (each waits for its predecessor
   // before reading what it wrote).  An event recorded between two kernels
   // (timing the main kernel alone) keeps them apart.
   e = launch_kernel(fa_bwd_main_kernel<D>, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, s, ev0 == nullptr, tq, tk, tv,
-                    tdo, tdq, p);
+                    tdo, tdq, pm);
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(pairs) * D / 8;

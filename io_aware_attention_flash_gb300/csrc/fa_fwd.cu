@@ -102,8 +102,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SeqPos sp = seq_pos(p.sv);
-  const int ctile = p.causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  int pair, tile;
+  cta_item(p.sv, pair, tile);
+  if (pair >= p.sv.npairs) return;
+  const SeqPos sp = seq_pos(p.sv, pair);
+  // Causal: the last query tiles see the most keys, so they go first.
+  const int ctile = p.causal ? p.sv.ntiles - 1 - tile : tile;
   const int q0 = ctile * kTile * NQT;
   if (q0 >= sp.seqlen) return;  // whole CTA past the end of a short packed sequence
 
@@ -490,8 +494,16 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(nseq * p.sv.H, (max_seqlen + kTile * C::NQT - 1) / (kTile * C::NQT));
-  fa_fwd_kernel<D, NQT><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, to, p);
+  int sms = 0;
+  cudaError_t e = current_sm_count(sms);
+  if (e != cudaSuccess) return e;
+  FwdParams pl = p;
+  pl.sv.npairs = nseq * p.sv.H;
+  pl.sv.ntiles = (max_seqlen + kTile * C::NQT - 1) / (kTile * C::NQT);
+  pl.sv.pair_group = pair_group_size(pl.sv.npairs, pl.sv.ntiles, sms * C::MIN_BLOCKS);
+  const long long ctas = grid_ctas(pl.sv.npairs, pl.sv.ntiles, pl.sv.pair_group);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fa_fwd_kernel<D, NQT><<<static_cast<unsigned>(ctas), C::NUM_THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, to, pl);
   return cudaGetLastError();
 }
 

@@ -21,7 +21,61 @@ struct SeqView {
   int H;
   int N;                  // dense: rows per sequence; packed: total rows
   int lse_stride;         // N (dense) or max_seqlen (packed)
+  int npairs;             // (sequence, head) pairs: nseq·H
+  int ntiles;             // tiles of the launch's kind along the longest sequence
+  int pair_group;         // pairs per launch group (pair_group_size)
 };
+
+// CTA order.  A CTA's work item is a (sequence·head pair, tile), and CTAs
+// start in increasing linear block index.  The items are launched in groups
+// of consecutive pairs: every tile of a group, tile-major in the kernel's
+// heaviest-first tile order, then the next group.  The CTAs in flight then
+// share the tiles of a few pairs in L2 (a packed batch with hundreds of
+// pairs would otherwise have nearly every CTA in flight on a pair of its
+// own).  A freed SM takes the next CTA, so starting each group's heavy tiles
+// first keeps the causal load balance as long as the groups are equal and
+// each spans at least two waves of CTAs; a short group, or a last group
+// smaller than the others, leaves heavy tiles for the end (greedy schedules
+// of the causal tile costs: 20-30 % longer).  Group size: the smallest
+// divisor of the pair count with at least two waves of tiles (searched up to
+// 4x that size); all pairs (plain tile-major order) when there is none.
+inline int pair_group_size(int npairs, int ntiles, int slots) {
+  const long long need = (2LL * slots + ntiles - 1) / ntiles;
+  for (long long g = need; g < npairs && g <= 4 * need; ++g)
+    if (npairs % g == 0) return static_cast<int>(g);
+  return npairs;
+}
+
+// Multiprocessors of the current device (cached per host thread).
+inline cudaError_t current_sm_count(int& sms) {
+  thread_local int cached_dev = -1, cached_sms = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != cached_dev) {
+    e = cudaDeviceGetAttribute(&cached_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cached_dev = dev;
+  }
+  sms = cached_sms;
+  return cudaSuccess;
+}
+
+inline long long grid_ctas(int npairs, int ntiles, int group) {
+  return static_cast<long long>((npairs + group - 1) / group) * group * ntiles;
+}
+
+// (pair, tile) of this CTA; pair >= sv.npairs marks a CTA of the last,
+// partial group with no work.
+__device__ __forceinline__ void cta_item(const SeqView& sv, int& pair, int& tile) {
+  const int g = sv.pair_group;
+  const int per_group = g * sv.ntiles;
+  const int b = static_cast<int>(blockIdx.x);
+  const int grp = b / per_group;
+  const int r = b - grp * per_group;
+  tile = r / g;
+  pair = grp * g + (r - tile * g);
+}
 
 struct FwdParams {
   SeqView sv;
@@ -68,15 +122,15 @@ struct DecodeParams {
   uint64_t timeout_ns;
 };
 
-// Position of a CTA's (sequence, head): blockIdx.x = sequence * H + head.
+// Position of a (sequence, head) pair: pair = sequence * H + head.
 struct SeqPos {
   int bs, h, seq_start, seqlen, row_base, tma_row0, tma_b;
 };
 
-__device__ __forceinline__ SeqPos seq_pos(const SeqView& sv) {
+__device__ __forceinline__ SeqPos seq_pos(const SeqView& sv, int pair) {
   SeqPos s;
-  s.bs = blockIdx.x / sv.H;
-  s.h = blockIdx.x % sv.H;
+  s.bs = pair / sv.H;
+  s.h = pair % sv.H;
   if (sv.cu_seqlens) {
     s.seq_start = __ldg(sv.cu_seqlens + s.bs);
     s.seqlen = __ldg(sv.cu_seqlens + s.bs + 1) - s.seq_start;
