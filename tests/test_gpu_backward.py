@@ -99,6 +99,49 @@ def test_backward_repeatable_and_workspace_reuse():
         assert rel_fro(f64(got), ref) <= GRAD_RTOL
 
 
+def test_backward_calls_back_to_back_share_a_workspace():
+    """Two backward calls on different inputs, queued with no synchronisation
+    in between and one workspace: the second call's pre-pass zeroes the fp32
+    accumulator that the first call's conversion reads, and each call's main
+    kernel may start before its pre-pass has finished (programmatic dependent
+    launch).  Both results against the oracle."""
+    fa = require_gpu()
+    B, N, H, d = 1, 515, 3, 128
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), device="cuda", dtype=torch.uint8)
+    runs = []
+    for seed in (21, 22):
+        q, k, v, do = wl.make_inputs(B, N, H, d, seed=seed)
+        qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+        o, lse = fa.attention_forward(qc, kc, vc, True)
+        runs.append(((q, k, v, do), fa.attention_backward(qc, kc, vc, o, doc, lse, True, workspace=ws)))
+    torch.cuda.synchronize()
+    assert_no_device_error(fa)
+    for (q, k, v, do), grads in runs:
+        ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, True)
+        for got, r in zip(grads, ref):
+            assert rel_fro(f64(got), r) <= GRAD_RTOL
+
+
+def test_backward_with_main_kernel_events():
+    """With the main kernel's own timing events requested, the backward's
+    kernels are launched one after another without overlap; same results,
+    and the events bracket a positive time."""
+    fa = require_gpu()
+    B, N, H, d = 2, 384, 2, 64
+    q, k, v, do = wl.make_inputs(B, N, H, d, seed=31)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention_forward(qc, kc, vc, False)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.fa_set_kernel_events(e0, e1)
+    grads = fa.attention_backward(qc, kc, vc, o, doc, lse, False)
+    torch.cuda.synchronize()
+    assert_no_device_error(fa)
+    assert e0.elapsed_time(e1) > 0
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, False)
+    for got, r in zip(grads, ref):
+        assert rel_fro(f64(got), r) <= GRAD_RTOL
+
+
 def test_autograd_function():
     fa = require_gpu()
     B, N, H, d = 1, 300, 2, 64
