@@ -63,7 +63,8 @@ enum {
   FA_ERR_NULL = 1,          /* a required pointer is NULL */
   FA_ERR_ALIGN = 2,         /* a pointer is not 16-byte aligned */
   FA_ERR_HEAD_DIM = 3,      /* d not in {64, 128} */
-  FA_ERR_SHAPE = 4,         /* B, H, N, nseq, total or max_seqlen out of range */
+  FA_ERR_SHAPE = 4,         /* B, H, N, nseq, total or max_seqlen out of range (among them: more
+                               than 2^31 - 1 (sequence, head, 128-row tile) triples) */
   FA_ERR_ARCH = 5,          /* current device is not compute capability 10.3 */
   FA_ERR_CUDA = 6,          /* a CUDA runtime/driver call or launch failed */
   FA_ERR_TIMEOUT = 7,       /* a kernel's bounded wait expired (device side) */
