@@ -21,6 +21,8 @@
 //                the fp32 accumulator by TMA bulk reduce-adds (other key tiles
 //                add to the same rows).
 //   fa_bwd_post  dQ = bf16(scale · dQ_accum).
+// Each launch may start while the previous one finishes (programmatic
+// dependent launch) and waits for it before touching what it wrote.
 // Warp roles in fa_bwd_main: warps 0-7 (two warpgroups, each owning half of
 // the query columns of a tile; thread r owns key row r = TMEM lane r)
 // recompute P and dS, drain dQ and write dK / dV; warp 8 issues TMA; warp 9
