@@ -390,9 +390,11 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
     user streaming batches would run it: every step's inputs go host->device
     and its O, LSE, dQ, dK, dV come back, all inside the timed region.  Steps
     are pipelined over three streams with double-buffered device tensors, so
-    step i+1's upload and step i-1's download overlap step i's kernels (each
-    step still waits for its own upload, and the L2 flush stays in front of
-    each step's kernels).  Returns the time per step of K steps."""
+    step i+1's upload and step i-1's download overlap step i's kernels.
+    Within a step the forward starts once Q, K, V are up (dO uploads under
+    it) and O, LSE go down while the backward runs, so neither direction of
+    the host link waits for a whole step (the L2 flush stays in front of each
+    step's kernels).  Returns the time per step of K steps."""
     hq, hk, hv, hdo = (t.pin_memory() for t in host_inputs)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     s_in, s_out, s_cmp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
@@ -403,7 +405,7 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
     d2h = sum(t.numel() * t.element_size() for t in host_out[0][0]) + host_out[0][1].numel() * 4
     wsp = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
     n = K + 2
-    ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(n)] for _ in range(3))
+    ev_qkv, ev_in, ev_fwd, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(n)] for _ in range(5))
 
     def one_step(i):
         b = i % 2
@@ -411,24 +413,31 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
         if i >= 2:
             s_in.wait_event(ev_cmp[i - 2])          # the step that last read these inputs has finished
         with torch.cuda.stream(s_in):
-            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            for dst, src in ((q, hq), (k, hk), (v, hv)):
                 dst.copy_(src, non_blocking=True)
+            ev_qkv[i].record(s_in)
+            do.copy_(hdo, non_blocking=True)
         ev_in[i].record(s_in)
-        s_cmp.wait_event(ev_in[i])
+        s_cmp.wait_event(ev_qkv[i])
         if i >= 2:
             s_cmp.wait_event(ev_out[i - 2])         # its output buffers have been read back
         with torch.cuda.stream(s_cmp):
             flush.zero_()
             o, lse = fa.attention_forward(q, k, v, w.causal, stream=s_cmp)
+            ev_fwd[i].record(s_cmp)
+            s_cmp.wait_event(ev_in[i])
             dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, w.causal, stream=s_cmp, workspace=wsp)
         dev_out[b] = (o, lse, dq, dk, dv)
         ev_cmp[i].record(s_cmp)
-        s_out.wait_event(ev_cmp[i])
         hosts, lse_h = host_out[b]
+        s_out.wait_event(ev_fwd[i])
         with torch.cuda.stream(s_out):
-            for dst, src in zip(hosts, (o, dq, dk, dv)):
-                dst.copy_(src, non_blocking=True)
+            hosts[0].copy_(o, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
+        s_out.wait_event(ev_cmp[i])
+        with torch.cuda.stream(s_out):
+            for dst, src in zip(hosts[1:], (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
             for t in dev_out[b]:
                 t.record_stream(s_out)
         ev_out[i].record(s_out)
@@ -444,7 +453,8 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
     t1.record(s_in)
     torch.cuda.synchronize(dev)
     return {"ms": t0.elapsed_time(t1) / K, "h2d": h2d, "d2h": d2h,
-            "note": "steps pipelined over 3 streams (upload / kernels / download), double-buffered"}
+            "note": "steps pipelined over 3 streams (upload / kernels / download), double-buffered; "
+                    "forward after Q, K, V are up, O and LSE down during the backward"}
 
 
 KERNEL_SOURCES = {
