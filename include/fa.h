@@ -256,6 +256,30 @@ FA_API fa_status fa_microbench(int which, int iters, double* result, void* strea
 FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event);
 
 /*
+ * Launch order of the attention kernels' CTAs (host only, needs no GPU; for
+ * inspection and tests).  Both the forward and the backward launch one CTA
+ * per (pair, tile) item, pair = sequence·H + head, tile = the kernel's tile
+ * index in its heaviest-first order under a causal mask (forward: query-tile
+ * groups from the last; backward: key tiles from the first), following the
+ * longest-processing-time-first scheduling of causal attention ("LLM Systems
+ * 22: Flash Attention", section 4.1.5).  CTAs start in launch order as SMs
+ * free up.  The items go in groups of `group` consecutive pairs: every tile
+ * of a group before the next group; within a group, tile by tile, pairs in
+ * order.  `group` is the smallest divisor of npairs whose group·ntiles items
+ * fill at least two waves of `slots` resident CTAs (searched up to four
+ * times that size), else npairs.  Launch configurations: the forward takes
+ * 256 query rows per tile at d = 128 (one CTA per SM) and 128 at d = 64 (two
+ * per SM); the backward 128 keys per tile, one CTA per SM.
+ *   npairs, ntiles, slots  positive; npairs·ntiles <= 2^31 − 1
+ *   group                  [out] the group size (may be NULL)
+ *   pair, tile             [out] host int arrays of `capacity` entries (may be
+ *                          NULL): the item of launch index b for b < capacity
+ * Returns FA_ERR_SHAPE for sizes out of range.
+ */
+FA_API fa_status fa_cta_order(int npairs, int ntiles, int slots, int* group, int* pair, int* tile,
+                              long long capacity);
+
+/*
  * Backward, dense batch, without a caller-supplied workspace.  (The pages
  * have no counterpart: this is a deployment convenience.)
  *

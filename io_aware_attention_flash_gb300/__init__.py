@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401  (C-ABI names)
     fa_bwd_varlen,
     fa_bwd_varlen_workspace_bytes,
     fa_bwd_workspace_bytes,
+    fa_cta_order,
     fa_fwd,
     fa_fwd_varlen,
     fa_get_device_error,

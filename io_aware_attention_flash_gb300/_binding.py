@@ -37,6 +37,7 @@ SIGNATURES = {
     "fa_get_device_error": (_I, [_P]),
     "fa_selftest_wait_timeout": (_I, [_U64, _P]),
     "fa_set_kernel_events": (_I, [_P, _P]),
+    "fa_cta_order": (_I, [_I, _I, _I, ctypes.POINTER(_I), _P, _P, ctypes.c_longlong]),
     "fa_last_error_detail": (ctypes.c_char_p, []),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_microbench": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double), _P]),
@@ -228,6 +229,20 @@ def fa_fwd_decode(q, k, v, o, lse, workspace, causal: bool, scale=None, stream=N
 
 def fa_get_device_error(stream=None) -> int:
     return int(lib().fa_get_device_error(_stream(stream)))
+
+
+def fa_cta_order(npairs: int, ntiles: int, slots: int):
+    """Launch order of the attention kernels' CTAs (host only): returns
+    (group, pair, tile) with pair[b], tile[b] the work item of launch index b."""
+    import numpy as np
+
+    group = ctypes.c_int(0)
+    _check("fa_cta_order", lib().fa_cta_order(npairs, ntiles, slots, ctypes.byref(group), None, None, 0))
+    n = -(-npairs // group.value) * group.value * ntiles
+    pair, tile = np.zeros(n, dtype=np.int32), np.zeros(n, dtype=np.int32)
+    _check("fa_cta_order", lib().fa_cta_order(npairs, ntiles, slots, None, pair.ctypes.data_as(_P),
+                                              tile.ctypes.data_as(_P), n))
+    return group.value, pair, tile
 
 
 def fa_set_kernel_events(start_event, end_event) -> None:

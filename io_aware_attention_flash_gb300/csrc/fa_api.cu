@@ -497,6 +497,25 @@ FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event) {
   return FA_OK;
 }
 
+FA_API fa_status fa_cta_order(int npairs, int ntiles, int slots, int* group, int* pair, int* tile,
+                              long long capacity) {
+  if (npairs <= 0 || ntiles <= 0 || slots <= 0) return FA_ERR_SHAPE;
+  if (static_cast<long long>(npairs) * ntiles > 0x7fffffffLL) return FA_ERR_SHAPE;
+  const int g = fa::pair_group_size(npairs, ntiles, slots);
+  if (group) *group = g;
+  const long long ctas = fa::grid_ctas(npairs, ntiles, g);
+  const long long n = capacity < ctas ? capacity : ctas;
+  // The kernels' decode of their linear block index (cta_item).
+  const long long per_group = static_cast<long long>(g) * ntiles;
+  for (long long b = 0; b < n; ++b) {
+    const long long grp = b / per_group, r = b - grp * per_group;
+    const long long t = r / g;
+    if (tile) tile[b] = static_cast<int>(t);
+    if (pair) pair[b] = static_cast<int>(grp * g + (r - t * g));
+  }
+  return FA_OK;
+}
+
 FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   FA_TRY(check_arch());
   uint32_t* err = nullptr;
