@@ -341,14 +341,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
           if (!reduce_tile(t)) break;
       }
       bulk_wait_group_read0();   // every reduce has read its slot; the adds land before the grid ends
-      if (*abort_flag) {
-        wait_drain(bar(C::B_K), 0, p.err, p.timeout_ns);
-        wait_drain(bar(C::B_V), 0, p.err, p.timeout_ns);
-        for (int s = 0; s < C::NSQ && s < fills; ++s) {
-          const uint32_t ph = ((s + ((fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1;
-          wait_drain(bar(C::B_QFULL + s), ph, p.err, p.timeout_ns);
-          wait_drain(bar(C::B_DOFULL + s), ph, p.err, p.timeout_ns);
-        }
+      // Every load this thread issued lands before the CTA may exit, whoever
+      // aborted and whenever (on a clean run these phases have all completed).
+      wait_drain(bar(C::B_K), 0, p.err, p.timeout_ns);
+      wait_drain(bar(C::B_V), 0, p.err, p.timeout_ns);
+      for (int s = 0; s < C::NSQ && s < fills; ++s) {
+        const uint32_t ph = ((s + ((fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1;
+        wait_drain(bar(C::B_QFULL + s), ph, p.err, p.timeout_ns);
+        wait_drain(bar(C::B_DOFULL + s), ph, p.err, p.timeout_ns);
       }
     }
   } else if (warp == C::MMA_WARP) {

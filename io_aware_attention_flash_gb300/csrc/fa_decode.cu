@@ -171,12 +171,14 @@ __global__ void __launch_bounds__(DecCfg<D, QG>::NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Unwinding: let every copy already issued land before the CTA exits.
-        for (int s = 0; s < C::NST && s < t; ++s) {
-          const int last = s + ((t - 1 - s) / C::NST) * C::NST;  // last tile issued into stage s
-          wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
-        }
+      // Every copy this thread issued lands before it exits, whoever aborted
+      // and whenever: this kernel has no CTA-wide barrier at its end, so once
+      // the compute warps have left (finished, or aborted after this loop
+      // issued its last tile) the CTA would retire with copies still writing
+      // into its shared memory.  On a clean run these phases have completed.
+      for (int s = 0; s < C::NST && s < t; ++s) {
+        const int last = s + ((t - 1 - s) / C::NST) * C::NST;  // last tile issued into stage s
+        wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
       }
     }
   } else {
@@ -447,11 +449,11 @@ __global__ void __launch_bounds__(DecMmaCfg::NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < C::NST && s < t; ++s) {
-          const int last = s + ((t - 1 - s) / C::NST) * C::NST;
-          wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
-        }
+      // As in the FMA kernel: every issued copy lands before the CTA-wide
+      // barrier at the end, whoever aborted and whenever.
+      for (int s = 0; s < C::NST && s < t; ++s) {
+        const int last = s + ((t - 1 - s) / C::NST) * C::NST;
+        wait_drain(bar(C::B_FULL + s), (last / C::NST) & 1, p.err, p.timeout_ns);
       }
     }
   } else if (warp == 5) {

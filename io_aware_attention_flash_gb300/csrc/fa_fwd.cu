@@ -210,17 +210,20 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
         load_v(j);
         ++v_fills;
       }
-      if (*abort_flag) {
-        // Unwinding: let every copy already issued land before the CTA exits.
-        for (int t = 0; t < NQT; ++t)
-          if (nkv[t] > 0) wait_drain(bar(C::B_Q + t), 0, p.err, p.timeout_ns);
-        for (int s = 0; s < C::NSK && s < k_fills; ++s)
-          wait_drain(bar(C::B_KFULL + s), ((s + ((k_fills - 1 - s) / C::NSK) * C::NSK) / C::NSK) & 1, p.err,
-                     p.timeout_ns);
-        for (int s = 0; s < C::NSV && s < v_fills; ++s)
-          wait_drain(bar(C::B_VFULL + s), ((s + ((v_fills - 1 - s) / C::NSV) * C::NSV) / C::NSV) & 1, p.err,
-                     p.timeout_ns);
-      }
+      // Every copy this thread issued lands before the CTA may exit, whoever
+      // aborted and whenever: a consumer can abort after this loop has issued
+      // its last load, and a CTA that exits with a copy still writing into its
+      // shared memory corrupts whatever the SM runs next.  On a clean run all
+      // of these phases have completed already (the MMA thread waited on
+      // them), so the waits return at once.
+      for (int t = 0; t < NQT; ++t)
+        if (nkv[t] > 0) wait_drain(bar(C::B_Q + t), 0, p.err, p.timeout_ns);
+      for (int s = 0; s < C::NSK && s < k_fills; ++s)
+        wait_drain(bar(C::B_KFULL + s), ((s + ((k_fills - 1 - s) / C::NSK) * C::NSK) / C::NSK) & 1, p.err,
+                   p.timeout_ns);
+      for (int s = 0; s < C::NSV && s < v_fills; ++s)
+        wait_drain(bar(C::B_VFULL + s), ((s + ((v_fills - 1 - s) / C::NSV) * C::NSV) / C::NSV) & 1, p.err,
+                   p.timeout_ns);
     }
   } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------------- MMA
