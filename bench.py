@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mid_n4096_d128] [--no-cpu-baseline] [--no-e2e]
+    python bench.py --dram-sweep [N ...]     (DRAM-traffic-vs-N driver for ncu)
 
 A step is one pass of the whole hot path over one batch: fa_fwd (one kernel)
 then fa_bwd (pre, main, post kernels).  Inputs are seeded synthetic bf16
@@ -485,6 +486,36 @@ def _committed_traffic(workload: str, kernel: str):
         return None
 
 
+def run_dram_sweep(args):
+    """One forward and one backward per sequence length, with B·H fixed, for
+    measuring how DRAM traffic grows with N under a profiler that reads the
+    DRAM byte counters (this mode times nothing itself).  IO-aware attention
+    keeps the N x N score matrix on chip, so its HBM traffic is O(N·d) per
+    head ("LLM Systems 22: Flash Attention", section 3.3; "08 ·
+    FlashAttention", section 三).  Prints the algorithmic minimum bytes per
+    call for each N, against which the measured counters are compared."""
+    import io_aware_attention_flash_gb300 as fa
+    from io_aware_attention_flash_gb300 import build as fabuild
+
+    if not torch.cuda.is_available():
+        raise SystemExit("--dram-sweep needs a CUDA device")
+    fabuild.build()
+    fa.load_library()
+    H, d = args.sweep_bh, 128
+    print("N,fwd_min_bytes,bwd_min_bytes", flush=True)
+    for N in args.dram_sweep:
+        q, k, v, do = (t.cuda() for t in wl.make_inputs(1, N, H, d, seed=args.seed))
+        o, lse = fa.attention_forward(q, k, v, causal=True)
+        fa.attention_backward(q, k, v, o, do, lse, causal=True)
+        torch.cuda.synchronize()
+        if fa.fa_get_device_error() != 0:
+            raise RuntimeError("device error in the DRAM sweep")
+        print(f"{N},{wl.min_hbm_bytes_fwd(H, d, N):.0f},{wl.min_hbm_bytes_bwd(H, d, N):.0f}", flush=True)
+        del q, k, v, do, o, lse
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -497,7 +528,15 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--dram-sweep", type=int, nargs="*", default=None, metavar="N",
+                    help="instead of the benchmark: one causal d=128 forward + backward per N (B=1, H=--sweep-bh), "
+                         "for a DRAM-counter capture; no N given: 1024 .. 32768")
+    ap.add_argument("--sweep-bh", type=int, default=8)
     args = ap.parse_args(argv)
+    if args.dram_sweep is not None:
+        if not args.dram_sweep:
+            args.dram_sweep = [1024, 2048, 4096, 8192, 16384, 32768]
+        return run_dram_sweep(args)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = wl.WORKLOADS[args.workload]

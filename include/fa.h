@@ -39,6 +39,11 @@
  *     no fallback path: an unsupported case is an error, never a slower
  *     route.  Device-side failures (a bounded wait that ran out) are reported
  *     by fa_get_device_error().
+ *   - Device state: per device, the library caches the device addresses of
+ *     its static device variables (the error word, the no-alloc scratch)
+ *     and the kernels' shared-memory limits, on first use.  A
+ *     cudaDeviceReset() invalidates them: do not use the library on a device
+ *     after resetting it in the same process.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -157,10 +162,12 @@ FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void
                                void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's error
- * word.  Returns FA_OK, FA_ERR_TIMEOUT (some kernel's bounded mbarrier wait
- * ran out and the kernel returned early: its outputs are invalid) or
- * FA_ERR_CUDA (the synchronisation itself failed).
+ * Synchronises `stream`, then reads and clears the error word of the device
+ * the stream belongs to (NULL, the legacy default stream: the current
+ * device); the calling thread's current device is left as it was.  Returns
+ * FA_OK, FA_ERR_TIMEOUT (some kernel's bounded mbarrier wait ran out and the
+ * kernel returned early: its outputs are invalid) or FA_ERR_CUDA (the
+ * synchronisation or the read itself failed).
  */
 FA_API fa_status fa_get_device_error(void* stream);
 
@@ -199,46 +206,14 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  *           9: the same with 64-column O tiles
  *          10: case 9 with P_t in TMEM columns that no MMA writes
  *          11: case 8 with both PV MMAs issued before both S MMAs
- *          12: bytes per SM-clock added into a 64 MiB fp32 array by TMA bulk
- *              reduce-adds of 32 x 32 fp32 chunks, 8 warps per SM, each
- *              staging its chunks through one 4 KB shared-memory slot (the
- *              backward's dQ drain); allocates and frees the array on
- *              `stream`
- *          13: case 12 with two slots per warp (two reduces in flight)
- *          14: the same additions as 16-byte vector atomics from registers
- *              (each lane its own row)
- *          15: case 14 with the array read as 128-row tiles, so that one
- *              warp instruction adds 512 contiguous bytes
- *          16: cases 12 and 15 at once, from half the warps each
- *          17: case 8 while two more warps on the issuing warp's SM
- *              sub-partition run a softmax-like FMA / ex2 loop
- *          18, 19, 20: case 8 with the issuing thread idle for 256, 600
- *              or 1200 cycles once per iteration (32 MMAs, 2048 cycles of
- *              tensor work): how much queued work covers a pause in issue
- *          21, 22: case 8 with a tcgen05.commit after each S (21) or after
- *              each PV and each S (22), to an mbarrier nobody waits on
- *          23: case 22 plus the forward kernel's four mbarrier waits per
- *              iteration, on an mbarrier whose phase is already complete
- *          24: case 23 with K and V taken from 3- and 2-slot rings
- *          25..30: SM cycles one thread spends on a synchronisation step
- *              (timed around the step and a branch on its result): 25
- *              mbarrier.try_wait on a completed phase, 26 the same plus
- *              tcgen05.fence::after_thread_sync, 27 mbarrier.test_wait, 28 a
- *              volatile shared-memory flag load, 29 tcgen05.commit, 30 the
- *              timer alone
- *          31..37: 25..29, the fence alone, and the timer alone, each right
- *              after the thread issued 16 MMAs (tensor queue full)
- *          38..41: exponentials per SM per clock in the softmax's per-pair
- *              step: 38 two ex2 + one cvt.rn.bf16x2.f32, 39 two ex2 + an
- *              integer bf16 pack, 40 the forward softmax's full step (paired
- *              FMA, ex2, paired add, cvt pack), 41 step 40 with the integer pack
+ *          38: exponentials per SM per clock in the softmax's per-pair step
+ *              with its bf16 packing: two ex2 + one cvt.rn.bf16x2.f32
+ *          40: the forward softmax's full per-pair step (paired FMA, two
+ *              ex2, paired add into the row sum, cvt pack), in exponentials
  *          42: largest relative difference of the polynomial exp2 (FMA pipe)
  *              from ex2.approx over [-30, 8]; -1 if a clamped input gave a
  *              negative, NaN or non-tiny value
  *          43: step 40 with a quarter of the pairs through the polynomial exp2
- *          44, 45: SM cycles for the forward softmax on one 128 x 128 score
- *              tile in TMEM with no MMA running, one tile (four warps, 44)
- *              or two tiles at once (eight warps, 45)
  * `iters` (1 .. 2^20) sets the loop length.  Returns FA_ERR_SHAPE for an
  * unknown `which` or out-of-range `iters`.
  */

@@ -45,7 +45,8 @@ SIGNATURES = {
     "fa_fwd_decode": (_I, [_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _F, _I, _P]),
 }
 
-# fa_microbench selectors: rate per SM per SM-clock of each unit.
+# fa_microbench selectors: rate per SM per SM-clock of each unit (the
+# MUFU-vs-tensor measurements), and the accuracy of the polynomial exp2.
 MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk": 2,
               "mma_bf16_flop_per_sm_clk_n256": 3, "mma_bf16_flop_per_sm_clk_n128": 4,
               "mma_bf16_flop_per_sm_clk_n128_tmem_a": 5, "mma_bf16_flop_per_sm_clk_n256_random": 6,
@@ -53,23 +54,8 @@ MICROBENCH = {"ex2_per_sm_clk": 0, "cvt_bf16x2_per_sm_clk": 1, "ffma_per_sm_clk"
               "fwd_mma_stream_flop_per_sm_clk_d128": 8, "fwd_mma_stream_flop_per_sm_clk_pv64": 9,
               "fwd_mma_stream_flop_per_sm_clk_pv64_separate_p": 10,
               "fwd_mma_stream_flop_per_sm_clk_d128_pv_first": 11,
-              "tma_reduce_bytes_per_sm_clk": 12, "tma_reduce_bytes_per_sm_clk_2slots": 13,
-              "red_v4_bytes_per_sm_clk": 14, "red_v4_coalesced_bytes_per_sm_clk": 15,
-              "tma_and_red_v4_bytes_per_sm_clk": 16, "fwd_mma_stream_flop_per_sm_clk_d128_busy": 17,
-              "fwd_mma_stream_flop_per_sm_clk_d128_gap256": 18, "fwd_mma_stream_flop_per_sm_clk_d128_gap600": 19,
-              "fwd_mma_stream_flop_per_sm_clk_d128_gap1200": 20,
-              "fwd_mma_stream_flop_per_sm_clk_d128_commit2": 21, "fwd_mma_stream_flop_per_sm_clk_d128_commit4": 22,
-              "fwd_mma_stream_flop_per_sm_clk_d128_waits": 23, "fwd_mma_stream_flop_per_sm_clk_d128_waits_ring": 24,
-              "sync_cycles_try_wait": 25, "sync_cycles_try_wait_fence": 26, "sync_cycles_test_wait": 27,
-              "sync_cycles_flag_load": 28, "sync_cycles_commit": 29, "sync_cycles_timer": 30,
-              "sync_cycles_try_wait_queue_full": 31, "sync_cycles_try_wait_fence_queue_full": 32,
-              "sync_cycles_test_wait_queue_full": 33, "sync_cycles_flag_load_queue_full": 34,
-              "sync_cycles_commit_queue_full": 35, "sync_cycles_fence_queue_full": 36,
-              "sync_cycles_timer_queue_full": 37,
-              "softmax_ex2_cvt_per_sm_clk": 38, "softmax_ex2_intpack_per_sm_clk": 39,
-              "softmax_step_per_sm_clk": 40, "softmax_step_intpack_per_sm_clk": 41,
-              "ex2_poly_max_rel_err": 42, "softmax_step_quarter_poly_per_sm_clk": 43,
-              "softmax_tile_cycles_1tile": 44, "softmax_tile_cycles_2tiles": 45}
+              "softmax_ex2_cvt_per_sm_clk": 38, "softmax_step_per_sm_clk": 40,
+              "ex2_poly_max_rel_err": 42, "softmax_step_quarter_poly_per_sm_clk": 43}
 
 # Size of the static scratch array behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -41,7 +41,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-constexpr int kMaxDevices = 64;
+using fa::kMaxDevices;
 
 // Text of the last FA_ERR_CUDA on this host thread (fa_last_error_detail).
 thread_local char t_detail[256] = "";
@@ -274,11 +274,16 @@ __global__ void fa_wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns
 }
 
 // Split-KV decode: keys per split and number of splits.  A split is 1 to 8
-// key tiles, sized so that there are about four work items per SM of a
-// GB300 (152 SMs) where the cache allows; the choice depends only on the
-// shapes, so the workspace size does too.
+// key tiles, sized so that there are about kDecodeTargetItems work items
+// where the cache allows.  The choice depends only on the shapes (not on the
+// device), so the workspace size does too; the persistent split kernel's grid
+// is sized from the SM count of the device it runs on.  608 is four items per
+// SM of a 152-SM part; on a part with a different SM count only the balance
+// of items over SMs changes, not the result.
+constexpr long long kDecodeTargetItems = 608;
+
 void decode_split(int B, int H, int Nk, int* splits, int* split_len) {
-  constexpr long long kTargetItems = 4 * 152;
+  constexpr long long kTargetItems = kDecodeTargetItems;
   const long long tiles = (Nk + fa::kTile - 1) / fa::kTile;
   long long per = (tiles * B * H + kTargetItems - 1) / kTargetItems;
   per = per < 1 ? 1 : (per > 8 ? 8 : per);
@@ -424,18 +429,36 @@ FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void
 }
 
 FA_API fa_status fa_get_device_error(void* stream) {
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  // The error word of the device the stream belongs to (the legacy default
+  // stream belongs to the current device); the caller's current device is
+  // restored afterwards.
+  int cur = 0, dev = 0;
+  if ((e = cudaGetDevice(&cur)) != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if ((e = cudaStreamGetDevice(s, &dev)) != cudaSuccess) return cuda_fail("cudaStreamGetDevice", e);
+  if (dev != cur && (e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail("cudaSetDevice", e);
   uint32_t word = 0;
-  if ((e = cudaMemcpyFromSymbol(&word, g_fa_error_word, sizeof(word))) != cudaSuccess)
-    return cuda_fail("read error word", e);
-  if (word == 0) return FA_OK;
-  const uint32_t zero = 0;
-  if ((e = cudaMemcpyToSymbol(g_fa_error_word, &zero, sizeof(zero))) != cudaSuccess)
-    return cuda_fail("clear error word", e);
-  if (word & fa::kDevErrTimeout) return FA_ERR_TIMEOUT;
-  snprintf(t_detail, sizeof(t_detail), "device error word 0x%x", word);
-  return FA_ERR_CUDA;
+  fa_status st = FA_OK;
+  if ((e = cudaMemcpyFromSymbol(&word, g_fa_error_word, sizeof(word))) != cudaSuccess) {
+    st = cuda_fail("read error word", e);
+  } else if (word != 0) {
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_fa_error_word, &zero, sizeof(zero))) != cudaSuccess) {
+      st = cuda_fail("clear error word", e);
+    } else if (word & fa::kDevErrTimeout) {
+      st = FA_ERR_TIMEOUT;
+    } else {
+      snprintf(t_detail, sizeof(t_detail), "device error word 0x%x", word);
+      st = FA_ERR_CUDA;
+    }
+  }
+  if (dev != cur) {
+    e = cudaSetDevice(cur);
+    if (st == FA_OK && e != cudaSuccess) st = cuda_fail("cudaSetDevice (restore)", e);
+  }
+  return st;
 }
 
 FA_API const char* fa_last_error_detail(void) { return t_detail; }
@@ -505,13 +528,11 @@ FA_API fa_status fa_cta_order(int npairs, int ntiles, int slots, int* group, int
   if (group) *group = g;
   const long long ctas = fa::grid_ctas(npairs, ntiles, g);
   const long long n = capacity < ctas ? capacity : ctas;
-  // The kernels' decode of their linear block index (cta_item).
-  const long long per_group = static_cast<long long>(g) * ntiles;
   for (long long b = 0; b < n; ++b) {
-    const long long grp = b / per_group, r = b - grp * per_group;
-    const long long t = r / g;
-    if (tile) tile[b] = static_cast<int>(t);
-    if (pair) pair[b] = static_cast<int>(grp * g + (r - t * g));
+    int pr = 0, t = 0;
+    fa::item_of_index(b, g, ntiles, pr, t);  // the kernels' own decode of their block index
+    if (tile) tile[b] = t;
+    if (pair) pair[b] = pr;
   }
   return FA_OK;
 }
@@ -528,29 +549,9 @@ FA_API fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 
 FA_API fa_status fa_microbench(int which, int iters, double* result, void* stream) {
   if (!result) return FA_ERR_NULL;
-  if (which < 0 || which > 45 || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
+  const bool known = (which >= 0 && which <= 11) || which == 38 || which == 40 || which == 42 || which == 43;
+  if (!known || iters <= 0 || iters > (1 << 20)) return FA_ERR_SHAPE;
   FA_TRY(check_arch());
-  if (which >= 12 && which <= 16) {
-    // Reduce-add throughput into a 64 MiB fp32 array shaped [8192, 16, 128].
-    constexpr int rows = 8192;
-    const size_t bytes = static_cast<size_t>(rows) * 16 * 128 * 4;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* buf = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&buf), bytes, s);
-    if (e != cudaSuccess) return cuda_fail("microbenchmark buffer", e);
-    fa_status st = FA_OK;
-    if ((e = cudaMemsetAsync(buf, 0, bytes, s)) != cudaSuccess) {
-      st = cuda_fail("microbenchmark buffer", e);
-    } else {
-      CUtensorMap tm;
-      st = make_map_dq(&tm, buf, 128, 16, rows);
-      if (st == FA_OK && (e = fa::run_reduce_microbench(which, iters, tm, buf, rows, result, s)) != cudaSuccess)
-        st = cuda_fail("microbenchmark", e);
-    }
-    const cudaError_t ef = cudaFreeAsync(buf, s);
-    if (st == FA_OK && ef != cudaSuccess) st = cuda_fail("microbenchmark buffer", ef);
-    return st;
-  }
   uint32_t* err = nullptr;
   FA_TRY(error_word(&err));
   const cudaError_t e = fa::run_microbench(which, iters, err, result, static_cast<cudaStream_t>(stream));

@@ -643,15 +643,11 @@ template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                          const CUtensorMap& tdq, const BwdParams& p, int max_seqlen, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = BwdCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit smem_limit;
+  cudaError_t e = smem_limit.ensure(reinterpret_cast<const void*>(fa_bwd_main_kernel<D>), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   int sms = 0;
-  cudaError_t e = current_sm_count(sms);
+  e = current_sm_count(sms);
   if (e != cudaSuccess) return e;
   BwdParams pm = p;
   pm.sv.npairs = p.nseq * p.sv.H;

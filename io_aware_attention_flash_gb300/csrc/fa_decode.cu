@@ -717,15 +717,12 @@ cudaError_t launch_decode_dq(const CUtensorMap& tk, const CUtensorMap& tv, const
                              cudaStream_t s) {
   constexpr int QG = NQ >= 2 ? 2 : 1;
   using C = DecCfg<D, QG>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_split_kernel<D, NQ, QG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit smem_limit;
+  cudaError_t e =
+      smem_limit.ensure(reinterpret_cast<const void*>(fa_decode_split_kernel<D, NQ, QG>), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   fa_decode_split_kernel<D, NQ, QG><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
   // Two warps per block: the rows are few (B·H·Nq), so spread them over the SMs.
@@ -739,15 +736,11 @@ template <int NQ>
 cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                               cudaStream_t s) {
   using C = DecMmaCfg;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_mma_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit smem_limit;
+  cudaError_t e = smem_limit.ensure(reinterpret_cast<const void*>(fa_decode_mma_kernel<NQ>), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   fa_decode_mma_kernel<NQ><<<grid, C::NUM_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = static_cast<long long>(p.B) * p.H * p.Nq;
   return launch_kernel(fa_decode_merge_kernel<C::D>, dim3(static_cast<unsigned>((warps * 32 + 63) / 64)), dim3(64), 0,

@@ -490,15 +490,11 @@ template <int D, int NQT>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                          const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s) {
   using C = FwdCfg<D, NQT>;
-  static bool configured = false;  // per process; attribute is per function
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_fwd_kernel<D, NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemLimit smem_limit;
+  cudaError_t e = smem_limit.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, NQT>), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   int sms = 0;
-  cudaError_t e = current_sm_count(sms);
+  e = current_sm_count(sms);
   if (e != cudaSuccess) return e;
   FwdParams pl = p;
   pl.sv.npairs = nseq * p.sv.H;

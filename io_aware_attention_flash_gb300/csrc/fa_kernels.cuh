@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -65,17 +66,49 @@ inline long long grid_ctas(int npairs, int ntiles, int group) {
   return static_cast<long long>((npairs + group - 1) / group) * group * ntiles;
 }
 
-// (pair, tile) of this CTA; pair >= sv.npairs marks a CTA of the last,
-// partial group with no work.
-__device__ __forceinline__ void cta_item(const SeqView& sv, int& pair, int& tile) {
-  const int g = sv.pair_group;
-  const int per_group = g * sv.ntiles;
-  const int b = static_cast<int>(blockIdx.x);
-  const int grp = b / per_group;
-  const int r = b - grp * per_group;
-  tile = r / g;
-  pair = grp * g + (r - tile * g);
+// Work item (pair, tile) of linear launch index b under groups of `group`
+// pairs of `ntiles` tiles each; pair >= npairs marks an index of the last,
+// partial group with no work.  The kernels decode their block index with it
+// and fa_cta_order reports the launch order with it on the host.
+__host__ __device__ __forceinline__ void item_of_index(long long b, int group, int ntiles, int& pair, int& tile) {
+  const long long per_group = static_cast<long long>(group) * ntiles;
+  const long long grp = b / per_group;
+  const long long r = b - grp * per_group;
+  tile = static_cast<int>(r / group);
+  pair = static_cast<int>(grp * group + (r - static_cast<long long>(tile) * group));
 }
+
+// (pair, tile) of this CTA.
+__device__ __forceinline__ void cta_item(const SeqView& sv, int& pair, int& tile) {
+  item_of_index(blockIdx.x, sv.pair_group, sv.ntiles, pair, tile);
+}
+
+constexpr int kMaxDevices = 64;
+
+// Raises a kernel's dynamic shared-memory limit above the 48 KB default.  The
+// attribute belongs to the current device, so it is set once per device (and
+// per kernel: one object per kernel instantiation), safely across host
+// threads.
+class SmemLimit {
+ public:
+  cudaError_t ensure(const void* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!done_[dev]) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e != cudaSuccess) return e;
+      done_[dev] = true;
+    }
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
 
 struct FwdParams {
   SeqView sv;
@@ -177,7 +210,5 @@ cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, c
                           cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t run_microbench(int which, int iters, uint32_t* err, double* result, cudaStream_t s);
-cudaError_t run_reduce_microbench(int which, int iters, const CUtensorMap& tm, float* buf, int rows, double* result,
-                                  cudaStream_t s);
 
 }  // namespace fa
