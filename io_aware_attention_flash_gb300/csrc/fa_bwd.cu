@@ -116,16 +116,35 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const BwdParams p, siz
 // fa_bwd_main
 // ----------------------------------------------------------------------------
 // TMEM holds dV and dK (d columns each) for the whole loop plus two 128-column
-// regions R0, R1 that alternate roles from one query tile to the next:
-//   tile i: Sᵀ_i -> R[i&1] (then Pᵀ_i as bf16, then dQ_i)
-//           dPᵀ_i -> R[(i+1)&1] (then dSᵀ_i as bf16)
-// so Sᵀ_{i+1} can be computed into R[(i+1)&1] as soon as dK_i has read dSᵀ_i,
-// while the compute warps drain dQ_i out of R[i&1]; dPᵀ_{i+1} then reuses
-// R[i&1].  MMA order per tile: dV_i, dK_i, dQ_i, Sᵀ_{i+1}, dPᵀ_{i+1}.  The
-// compute warps overlap Pᵀ_{i+1} with dPᵀ_{i+1}, dSᵀ_{i+1} with dV_{i+1}, and
-// the dQ_i drain with Sᵀ_{i+1}.
+// regions with fixed roles:
+//   X: Sᵀ_i, then Pᵀ_i as bf16 (the A operand of dV_i)
+//   Y: dPᵀ_i, then dQ_i
+// dSᵀ_i goes to shared memory only: it is the A operand of both dQ_i (read
+// MN-major, as dS) and dK_i (read K-major, as dSᵀ).  MMA order per tile:
+// dV_i, Sᵀ_{i+1}, dQ_i, dK_i, dPᵀ_{i+1}.  Sᵀ_{i+1} overwrites Pᵀ_i right
+// after dV_i has read it, so the compute warps form Pᵀ_{i+1} while the tensor
+// pipe runs dQ_i and dK_i; dQ_i comes before dK_i so that its drain starts as
+// early as possible; dPᵀ_{i+1} overwrites dQ_i once the drain warps have read
+// it out of TMEM.  (MMAs issued by one thread execute in issue order, so each
+// overwrite follows the read before it.)
+//
+// Shared memory and the dQ read-out.  A tile's fp32 dQ (64 KB at d = 128)
+// leaves the SM through bulk reduce-adds at the SM's reduction egress rate
+// (about 25 bytes per clock, measured alike for one SM and for all of them,
+// and shared by the TMA and vector-atomic paths), so its read-out lasts about
+// as long as the tile's five GEMMs, and whatever shared memory holds it is
+// tied up meanwhile.  dQ is therefore staged in a buffer of its own (STG),
+// never over a Q/dO ring slot that the next tiles' loads need:
+//   d = 128: the dS operand of the dQ GEMM is written over the tile's dO
+//            (consumed once dPᵀ_i and dV_i have completed), which frees the
+//            32 KB that a separate dS buffer would take for STG; dQ columns
+//            0-63 go to STG and columns 64-127 over that dS.  A slot's Q is
+//            reloaded as soon as dK_i has read it, its dO once the half of dQ
+//            over it has been read out.
+//   d = 64:  a separate dS buffer and a 32 KB STG that holds all of dQ.
 template <int D>
 struct BwdCfg {
+  static constexpr bool DS_IN_DO = (D == 128);         // dS written over the tile's consumed dO
   static constexpr int KB = D / 64;
   static constexpr int BLK_BYTES = kTile * 128;        // 128 rows x 64 bf16
   static constexpr int TILE_BYTES = KB * BLK_BYTES;    // 128 x D bf16
@@ -134,17 +153,24 @@ struct BwdCfg {
   static constexpr int OFF_V = OFF_K + TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + TILE_BYTES;
   static constexpr int OFF_DO = OFF_Q + NSQ * TILE_BYTES;
-  static constexpr int OFF_DS = OFF_DO + NSQ * TILE_BYTES;      // dSᵀ, 128 key rows x 128 q, 2 blocks
-  static constexpr int OFF_STAT = OFF_DS + 2 * BLK_BYTES;       // [2][2][128] fp32: log2e·LSE and D
+  // dSᵀ, 128 key rows x 128 queries in two 64-query blocks (d = 64 only)
+  static constexpr int OFF_DS = OFF_DO + NSQ * TILE_BYTES;
+  static constexpr int OFF_STG = OFF_DS + (DS_IN_DO ? 0 : 2 * BLK_BYTES);  // dQ staging, 32 KB
+  static constexpr int STG_BYTES = 32768;
+  static constexpr int OFF_STAT = OFF_STG + STG_BYTES;  // [2][2][128] fp32: log2e·LSE and D
   static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * kTile * 4;
   static constexpr int B_K = 0;
   static constexpr int B_V = 1;
   static constexpr int B_QFULL = 2;
   static constexpr int B_DOFULL = B_QFULL + NSQ;
-  // B_STAGED[s]: the drain warps have staged the dQ of the query tile in
-  // ring slot s over that tile's (consumed) Q and dO.
-  static constexpr int B_STAGED = B_DOFULL + NSQ;
-  static constexpr int B_SFULL = B_STAGED + NSQ;
+  // [NSQ]: dK of the slot's tile has read its Q and dS (both the slot's Q and,
+  // at d = 128, the dS over its dO may be overwritten)
+  static constexpr int B_QFREE = B_DOFULL + NSQ;
+  static constexpr int B_DOFREE = B_QFREE + NSQ;       // [NSQ] (d = 64): dV of the slot's tile has read its dO
+  static constexpr int B_STAGED = B_DOFREE + NSQ;      // the drain warps have staged a tile's dQ
+  static constexpr int B_STGFREE = B_STAGED + 1;       // the reduces have read STG
+  static constexpr int B_DVDONE = B_STGFREE + 1;       // (d = 128) dV_i has read dO_i: dS may go over it
+  static constexpr int B_SFULL = B_DVDONE + 1;
   static constexpr int B_DPFULL = B_SFULL + 1;
   static constexpr int B_PREADY = B_DPFULL + 1;
   static constexpr int B_DSREADY = B_PREADY + 1;
@@ -159,11 +185,18 @@ struct BwdCfg {
   // Whatever is left of the 227 KB opt-in limit is alignment slack.
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
   static constexpr int NCHT = D / 32;                  // 32-column dQ chunks per row
-  // Staging slice (32 rows x 32 fp32 columns, 4 KB) of dQ rows 32·wq .. +31,
-  // columns 32·c .. +31, for the tile in ring slot qs: the first half of the
-  // chunks over the tile's Q, the second half over its dO.
-  __host__ __device__ static constexpr uint32_t dq_slot(int qs, int c, int wq) {
-    return (c < NCHT / 2 ? OFF_Q : OFF_DO) + qs * TILE_BYTES + ((c % (NCHT / 2)) * 4 + wq) * 4096;
+  static constexpr int NCH_STG = 2;                    // chunks 0, 1 are staged in STG
+  static_assert(kTile * NCH_STG * 32 * 4 == STG_BYTES, "STG holds two 32-column chunks of a tile");
+  // Byte offset of the staging slice (32 rows x 32 fp32 columns, 4 KB,
+  // 128-byte swizzled) of dQ rows 32·wq .. +31, columns 32·c .. +31, for the
+  // tile in ring slot qs.
+  __host__ __device__ static constexpr uint32_t dq_slice(int qs, int c, int wq) {
+    return c < NCH_STG ? OFF_STG + (c * 4 + wq) * 4096
+                       : OFF_DO + qs * TILE_BYTES + ((c - NCH_STG) * 4 + wq) * 4096;
+  }
+  // Base of the dSᵀ tile of the query tile in ring slot qs.
+  __host__ __device__ static constexpr uint32_t ds_base(int qs) {
+    return DS_IN_DO ? OFF_DO + qs * TILE_BYTES : OFF_DS;
   }
   static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
   static constexpr int NUM_DRAIN = 128;                // warps 10-13: one per TMEM lane quarter
@@ -180,8 +213,10 @@ struct BwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t DV_COL = 0;
   static constexpr uint32_t DK_COL = D;
-  static constexpr uint32_t R_COL = 2 * D;             // R0 = R_COL, R1 = R_COL + 128
+  static constexpr uint32_t R_COL = 2 * D;             // X = R_COL, Y = R_COL + 128
   static_assert(SMEM_USED <= 232448, "shared memory budget");
+  static_assert(!DS_IN_DO || TILE_BYTES == 2 * BLK_BYTES, "dSᵀ (two 64-query blocks) fits over a dO tile");
+  static_assert(!DS_IN_DO || (NCHT - NCH_STG) * 4 * 4096 <= TILE_BYTES, "dQ half fits over a dO tile");
 };
 
 template <int D>
@@ -235,10 +270,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       tma_load_4d(sb + C::OFF_DO + qs * C::TILE_BYTES + kb * C::BLK_BYTES, &tmdO, bar(C::B_DOFULL + qs), kb * 64,
                   sp.h, qrow, sp.tma_b);
   };
-  auto load_qdo = [&](int ii) {
-    load_q(ii);
-    load_do(ii);
-  };
   // K, V and the query tiles whose ring slots start empty are loaded by the
   // producer as soon as it has initialised the barriers, so the first loads
   // overlap the TMEM allocation and the CTA-wide barrier.
@@ -250,8 +281,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     for (int s = 0; s < C::NSQ; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1);
       mbar_init(bar(C::B_DOFULL + s), 1);
-      mbar_init(bar(C::B_STAGED + s), C::NUM_DRAIN);
+      mbar_init(bar(C::B_QFREE + s), 1);
+      mbar_init(bar(C::B_DOFREE + s), 1);
     }
+    mbar_init(bar(C::B_STAGED), C::NUM_DRAIN);
+    mbar_init(bar(C::B_STGFREE), 1);
+    mbar_init(bar(C::B_DVDONE), 1);
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PREADY), C::NUM_COMPUTE);
@@ -279,7 +314,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     for (int kb = 0; kb < C::KB; ++kb)
       tma_load_4d(sb + C::OFF_V + kb * C::BLK_BYTES, &tmV, bar(C::B_V), kb * 64, sp.h, sp.tma_row0 + kv0, sp.tma_b);
     if (preloaded > 0) load_do(0);
-    for (int ii = 1; ii < preloaded; ++ii) load_qdo(ii);
+    for (int ii = 1; ii < preloaded; ++ii) {
+      load_q(ii);
+      load_do(ii);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -296,67 +334,74 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     // ---------------------------------------------------------------- TMA
     setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
-      // The dQ of query tile t is staged (fp32, 128-byte swizzled, one 4 KB
-      // slice per 32 rows and 32 columns: columns 0-63 over Q_t, 64-127 over
-      // dO_t) in ring slot t % NSQ once the MMAs have consumed them.  This
-      // thread adds the slices into the accumulator with TMA bulk reduce-adds
-      // and reuses the slot for tile t + NSQ once the reduces have read it.
-      // The reduces read at the L2's reduce rate, so a slot takes thousands of
-      // cycles to empty: the half over Q_t goes first, in its own bulk group,
-      // and Q_{t+NSQ} (needed first, for Sᵀ) is loaded as soon as that half
-      // has been read, dO_{t+NSQ} after the other half.
-      auto reduce_half = [&](int t, int half) {
+      // Per query tile t (ring slot s): reload Q of tile t + NSQ into s once
+      // dK_t has read Q_t; add the staged dQ_t into the accumulator (TMA bulk
+      // reduce-adds, the STG part first, so that the drain of tile t + 1 can
+      // reuse STG); reload dO of tile t + NSQ once nothing reads the slot's
+      // dO region any more (d = 128: the half of dQ_t staged over it has been
+      // read; d = 64: dV_t has read dO_t).
+      auto reduce_chunks = [&](int t, int c_lo, int c_hi) {
         const int qs = t % C::NSQ;
         const int q0 = (i_first + t) * kTile;
 #pragma unroll 1
         for (int wq = 0; wq < 4; ++wq) {
 #pragma unroll
-          for (int c = half * (C::NCHT / 2); c < (half + 1) * (C::NCHT / 2); ++c)
-            tma_reduce_add_3d(&tmDQ, sb + C::dq_slot(qs, c, wq), 32 * c, sp.h, sp.row_base + q0 + 32 * wq);
+          for (int c = c_lo; c < c_hi; ++c)
+            tma_reduce_add_3d(&tmDQ, sb + C::dq_slice(qs, c, wq), 32 * c, sp.h, sp.row_base + q0 + 32 * wq);
         }
         bulk_commit_group();
-      };
-      auto reduce_tile = [&](int t) -> bool {
-        const int qs = t % C::NSQ;
-        if (!wait_bounded(bar(C::B_STAGED + qs), (t / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) return false;
-        reduce_half(t, 0);
-        reduce_half(t, 1);
-        return true;
       };
       // The first reduce-add needs the accumulator zeroed by the pre-pass
       // (plain stores, possibly still running when this kernel started).
       grid_dependency_wait();
       fence_proxy_async_global();
-      int fills = preloaded;
-      for (int ii = preloaded; ii < nq; ++ii) {
-        if (!reduce_tile(ii - C::NSQ)) break;
-        bulk_wait_group_read<1>();  // the half over Q has been read
-        load_q(ii);
-        bulk_wait_group_read0();    // and the half over dO
-        load_do(ii);
-        ++fills;
+      int q_fills = preloaded, do_fills = preloaded;
+      for (int t = 0; t < nq; ++t) {
+        const int s = t % C::NSQ;
+        const int nxt = t + C::NSQ;
+        const uint32_t ph = (t / C::NSQ) & 1;
+        if (nxt < nq) {
+          if (!wait_bounded(bar(C::B_QFREE + s), ph, abort_flag, p.err, p.timeout_ns)) break;
+          load_q(nxt);
+          ++q_fills;
+        }
+        if (!wait_bounded(bar(C::B_STAGED), t & 1, abort_flag, p.err, p.timeout_ns)) break;
+        reduce_chunks(t, 0, C::NCH_STG);
+        if constexpr (C::NCHT > C::NCH_STG) {
+          reduce_chunks(t, C::NCH_STG, C::NCHT);
+          bulk_wait_group_read<1>();   // STG has been read
+        } else {
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(bar(C::B_STGFREE));
+        if (nxt < nq) {
+          if constexpr (C::DS_IN_DO) {
+            bulk_wait_group_read0();   // the half of dQ over the dO region has been read
+          } else {
+            if (!wait_bounded(bar(C::B_DOFREE + s), ph, abort_flag, p.err, p.timeout_ns)) break;
+          }
+          load_do(nxt);
+          ++do_fills;
+        }
       }
-      if (!*abort_flag) {
-        for (int t = (nq > C::NSQ ? nq - C::NSQ : 0); t < nq; ++t)
-          if (!reduce_tile(t)) break;
-      }
-      bulk_wait_group_read0();   // every reduce has read its slot; the adds land before the grid ends
+      bulk_wait_group_read0();   // every reduce has read its source; the adds land before the grid ends
       // Every load this thread issued lands before the CTA may exit, whoever
       // aborted and whenever (on a clean run these phases have all completed).
       wait_drain(bar(C::B_K), 0, p.err, p.timeout_ns);
       wait_drain(bar(C::B_V), 0, p.err, p.timeout_ns);
-      for (int s = 0; s < C::NSQ && s < fills; ++s) {
-        const uint32_t ph = ((s + ((fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1;
-        wait_drain(bar(C::B_QFULL + s), ph, p.err, p.timeout_ns);
-        wait_drain(bar(C::B_DOFULL + s), ph, p.err, p.timeout_ns);
-      }
+      for (int s = 0; s < C::NSQ && s < q_fills; ++s)
+        wait_drain(bar(C::B_QFULL + s), ((s + ((q_fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1, p.err,
+                   p.timeout_ns);
+      for (int s = 0; s < C::NSQ && s < do_fills; ++s)
+        wait_drain(bar(C::B_DOFULL + s), ((s + ((do_fills - 1 - s) / C::NSQ) * C::NSQ) / C::NSQ) & 1, p.err,
+                   p.timeout_ns);
     }
   } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------------- MMA
     setmaxnreg_dec<C::REG_OTHER>();
     if (lane == 0) {
       constexpr uint32_t idesc_sp = idesc_bf16(128, 128, false, false);   // Sᵀ, dPᵀ
-      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);      // dV, dK (A from TMEM)
+      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);      // dV (A from TMEM), dK
       constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);        // dQ (A = dS, MN-major)
       auto region = [&](int r) -> uint32_t { return tmem + C::R_COL + (r & 1) * 128; };
       // Tile-base descriptors, K-major (k steps of 32 bytes within a
@@ -366,7 +411,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
       const uint64_t mnQ = sdesc_sw128(sb + C::OFF_Q, C::BLK_BYTES, 1024);
       const uint64_t mnDO = sdesc_sw128(sb + C::OFF_DO, C::BLK_BYTES, 1024);
       const uint64_t mnK = sdesc_sw128(sb + C::OFF_K, C::BLK_BYTES, 1024);
-      const uint64_t mnDS = sdesc_sw128(sb + C::OFF_DS, C::BLK_BYTES, 1024);
       auto issue_sp = [&](uint32_t dst, uint64_t a, uint64_t b) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -378,52 +422,61 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 wait_bounded(bar(C::B_QFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       if (ok) {
         tc_fence_after();
-        issue_sp(region(0), kmK, kmQ);                                     // Sᵀ_0 -> R0
+        issue_sp(region(0), kmK, kmQ);                                     // Sᵀ_0 -> X
         tc_commit(bar(C::B_SFULL));
         ok = wait_bounded(bar(C::B_V), 0, abort_flag, p.err, p.timeout_ns) &&
              wait_bounded(bar(C::B_DOFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
       }
       if (ok) {
         tc_fence_after();
-        issue_sp(region(1), kmV, kmDO);                                    // dPᵀ_0 -> R1
+        issue_sp(region(1), kmV, kmDO);                                    // dPᵀ_0 -> Y
         tc_commit(bar(C::B_DPFULL));
       }
+      const uint32_t tX = region(0), tY = region(1);
       for (int ii = 0; ok && ii < nq; ++ii) {
         const int qs = ii % C::NSQ;
         const uint64_t bQ = sdesc_add(mnQ, qs * C::TILE_BYTES), bdO = sdesc_add(mnDO, qs * C::TILE_BYTES);
-        const uint32_t rs = region(ii), rp = region(ii + 1);
+        const uint64_t aDS = sdesc_sw128(sb + C::ds_base(qs), C::BLK_BYTES, 1024);  // dS, MN-major
+        const uint64_t kDS = sdesc_sw128(sb + C::ds_base(qs), 16, 1024);            // dSᵀ, K-major
+        const bool next = ii + 1 < nq;
+        const int qs1 = (ii + 1) % C::NSQ;
+        const uint32_t ph1 = ((ii + 1) / C::NSQ) & 1;
         ok = wait_bounded(bar(C::B_PREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)  // dV += Pᵀ dO_i (Pᵀ packed in rs)
-          mma_ts(tmem + C::DV_COL, rs + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bdO, kk * 2048), idesc_kv,
+        for (int kk = 0; kk < kTile / 16; ++kk)  // dV += Pᵀ dO_i (Pᵀ packed in X)
+          mma_ts(tmem + C::DV_COL, tX + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bdO, kk * 2048), idesc_kv,
                  (ii > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::DS_IN_DO ? C::B_DVDONE : C::B_DOFREE + qs));  // dO_i read: dS (or the next dO) may go there
+        if (next) {
+          ok = wait_bounded(bar(C::B_QFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sp(tX, kmK, sdesc_add(kmQ, qs1 * C::TILE_BYTES));               // Sᵀ_{i+1} -> X (after dV_i)
+          tc_commit(bar(C::B_SFULL));
+        }
         ok = wait_bounded(bar(C::B_DSREADY), ii & 1, abort_flag, p.err, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dSᵀ Q_i (dSᵀ packed in rp)
-          mma_ts(tmem + C::DK_COL, rp + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bQ, kk * 2048), idesc_kv,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)  // dQ_i = dS K_j -> rs
-          mma_ss(rs, sdesc_add(mnDS, kk * 2048), sdesc_add(mnK, kk * 2048), idesc_q, kk > 0);
+        for (int kk = 0; kk < kTile / 16; ++kk)  // dQ_i = dS K_j -> Y (dPᵀ_i read by the compute warps)
+          mma_ss(tY, sdesc_add(aDS, kk * 2048), sdesc_add(mnK, kk * 2048), idesc_q, kk > 0);
         tc_commit(bar(C::B_DQFULL));
-        if (ii + 1 < nq) {
-          const int qs1 = (ii + 1) % C::NSQ;
-          const uint32_t ph1 = ((ii + 1) / C::NSQ) & 1;
-          ok = wait_bounded(bar(C::B_QFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          issue_sp(rp, kmK, sdesc_add(kmQ, qs1 * C::TILE_BYTES));               // Sᵀ_{i+1} -> rp
-          tc_commit(bar(C::B_SFULL));
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {  // dK += dSᵀ Q_i (dSᵀ K-major from shared memory)
+          const uint32_t koff = (kk / 4) * C::BLK_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + C::DK_COL, sdesc_add(kDS, koff), sdesc_add(bQ, kk * 2048), idesc_kv,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_QFREE + qs));          // Q_i and dS_i read: the slot may be reused
+        if (next) {
           ok = wait_bounded(bar(C::B_DQDRAINED), ii & 1, abort_flag, p.err, p.timeout_ns);
           if (!ok) break;
           ok = wait_bounded(bar(C::B_DOFULL + qs1), ph1, abort_flag, p.err, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          issue_sp(rs, kmV, sdesc_add(kmDO, qs1 * C::TILE_BYTES));              // dPᵀ_{i+1} -> rs
+          issue_sp(tY, kmV, sdesc_add(kmDO, qs1 * C::TILE_BYTES));              // dPᵀ_{i+1} -> Y
           tc_commit(bar(C::B_DPFULL));
         }
       }
@@ -438,10 +491,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     setmaxnreg_dec<C::REG_OTHER>();
     // One warp per TMEM lane quarter wq (dQ rows 32·wq .. +31 of the query
     // tile; thread = row).  Once dQ_i has completed, copy the rows from TMEM
-    // into the 128-byte swizzled staging slices over Q_i / dO_i, two 32-column
-    // chunks at a time, release the TMEM region to the MMA warp and hand the
-    // slices to the TMA producer, which adds them into the accumulator.  Rows
-    // past the sequence end carry exact zeros (their P, hence dS, is 0).
+    // into the 128-byte swizzled staging slices, two 32-column chunks at a
+    // time: first, once the reduces of tile i − 1 have read STG, the chunks
+    // that go to STG; then (d = 128) the other chunks, which go over the
+    // tile's dS: they are read out of TMEM at once, so the TMEM region is
+    // released to the MMA warp, and stored once dK_i has finished reading dS.
+    // Then the slices are handed to the TMA producer, which adds them into
+    // the accumulator.  Rows past the sequence end carry exact zeros (their
+    // P, hence dS, is 0).
     const int wq = warp & 3;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     auto stage_chunk = [&](const uint32_t (&v)[32], uint32_t slice) {
@@ -453,26 +510,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                      : "memory");
       }
     };
+    auto load_pair = [&](uint32_t rs, int c0, uint32_t (&a)[2][32]) {
+      tmem_ld32(rs + 32 * c0, a[0]);
+      tmem_ld32(rs + 32 * (c0 + 1), a[1]);
+      tmem_wait_ld();
+      reg_fence(a[0]);
+      reg_fence(a[1]);
+    };
+    static_assert(C::NCHT - C::NCH_STG <= 2, "at most one chunk pair is staged over dS");
     for (int ii = 0; ii < nq; ++ii) {
-      const uint32_t rs = lane_addr + C::R_COL + (ii & 1) * 128;
+      const uint32_t rs = lane_addr + C::R_COL + 128;  // dQ_i in region Y
       if (!wait_bounded(bar(C::B_DQFULL), ii & 1, abort_flag, p.err, p.timeout_ns)) break;
       tc_fence_after();
       const int qs = ii % C::NSQ;
+      if (ii > 0 && !wait_bounded(bar(C::B_STGFREE), (ii - 1) & 1, abort_flag, p.err, p.timeout_ns)) break;
+      uint32_t a[2][32];
 #pragma unroll
-      for (int c0 = 0; c0 < C::NCHT; c0 += 2) {
-        uint32_t a[2][32];
-        tmem_ld32(rs + 32 * c0, a[0]);
-        tmem_ld32(rs + 32 * (c0 + 1), a[1]);
-        tmem_wait_ld();
-        reg_fence(a[0]);
-        reg_fence(a[1]);
-        stage_chunk(a[0], sb + C::dq_slot(qs, c0, wq));
-        stage_chunk(a[1], sb + C::dq_slot(qs, c0 + 1, wq));
+      for (int c0 = 0; c0 < C::NCH_STG; c0 += 2) {
+        load_pair(rs, c0, a);
+        stage_chunk(a[0], sb + C::dq_slice(qs, c0, wq));
+        stage_chunk(a[1], sb + C::dq_slice(qs, c0 + 1, wq));
+      }
+      if constexpr (C::NCHT > C::NCH_STG) {
+        if (!wait_bounded(bar(C::B_QFREE + qs), (ii / C::NSQ) & 1, abort_flag, p.err, p.timeout_ns)) break;
+        load_pair(rs, C::NCH_STG, a);
+        stage_chunk(a[0], sb + C::dq_slice(qs, C::NCH_STG, wq));
+        stage_chunk(a[1], sb + C::dq_slice(qs, C::NCH_STG + 1, wq));
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DQDRAINED));
       fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_STAGED + qs));
+      mbar_arrive(bar(C::B_STAGED));
     }
   } else {
     // ---------------------------------------------------------------- P, dS
@@ -489,31 +557,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     const bool row_dead = kv_row >= sp.seqlen;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
-    // log2e·LSE (warpgroup 0; +inf past the sequence end, so P = 0 there) or
-    // D (warpgroup 1) of query row r of tile ii.
+    // LSE (warpgroup 0; +inf past the sequence end, so P = 0 there) or D
+    // (warpgroup 1) of query row r of tile ii, as loaded: the value is first
+    // used a whole tile later, when it is published, so nothing waits for the
+    // load before then (scaling it by log2 e here would stall the warp for
+    // the load's latency on every tile).
     auto load_stat = [&](int ii) -> float {
       const int q = (i_first + ii) * kTile + r;
       if (q >= sp.seqlen) return g == 0 ? CUDART_INF_F : 0.f;
-      return g == 0 ? __ldg(p.lse + stat_base + q) * kLog2e : __ldg(p.dpsum + stat_base + q);
+      return __ldg((g == 0 ? p.lse : p.dpsum) + stat_base + q);
     };
-    // Both warpgroups read all 128 entries of a tile: publish them through an
-    // mbarrier (a bounded wait, unlike a named barrier, so an abort cannot
-    // hang).  Buffer ii & 1 was last read during tile ii - 2, which every
-    // thread has finished once it has passed tile ii - 1's wait.
+    // Both warpgroups read all 128 entries of a tile (log2e·LSE and D):
+    // publish them through an mbarrier (a bounded wait, unlike a named
+    // barrier, so an abort cannot hang).  Buffer ii & 1 was last read during
+    // tile ii - 2, which every thread has finished once it has passed tile
+    // ii - 1's wait.
     auto publish_stat = [&](int ii, float v) {
       float* buf = stat + (ii & 1) * 256;
-      buf[g * 128 + r] = v;
+      buf[g * 128 + r] = g == 0 ? v * kLog2e : v;
       mbar_arrive(bar(C::B_STAT + (ii & 1)));
     };
     grid_dependency_wait();  // D comes from the pre-pass
     if (nq > 0) publish_stat(0, load_stat(0));
+    // stat_next: tile ii + 1's value, published at the end of tile ii; the
+    // load of tile ii + 2's is issued at the top of tile ii, before this
+    // thread's shared-memory stores of the tile (a load queued behind them
+    // waits for them to drain).
     float stat_next = nq > 1 ? load_stat(1) : 0.f;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
+      const float stat_after = ii + 2 < nq ? load_stat(ii + 2) : 0.f;
       const int qi = i_first + ii;
       const int q0 = qi * kTile;
-      const uint32_t rs = lane_addr + C::R_COL + (ii & 1) * 128;
-      const uint32_t rp = lane_addr + C::R_COL + ((ii + 1) & 1) * 128;
+      const uint32_t rs = lane_addr + C::R_COL;        // region X: Sᵀ, Pᵀ
+      const uint32_t rp = lane_addr + C::R_COL + 128;  // region Y: dPᵀ
       const float* lse2 = stat + (ii & 1) * 256;
       const float* dsum = lse2 + 128;
       if (!wait_bounded(bar(C::B_STAT + (ii & 1)), (ii >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
@@ -568,6 +645,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
+      // dSᵀ row r, this warpgroup's 64 query columns -> the swizzled SMEM
+      // block g (the A operand of dQ_i, MN-major, and of dK_i, K-major); at
+      // d = 128 that block lies over the tile's dO, which dV_i must have
+      // finished reading first.
+      const uint32_t rowaddr = sb + C::ds_base(ii % C::NSQ) + g * C::BLK_BYTES + r * 128;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dp[32];
@@ -582,9 +664,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
           const float d1 = __uint_as_float(pr[ch][2 * e + 1]) * (__uint_as_float(dp[2 * e + 1]) - dsum[col + 1]);
           dk[e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(rp + 64 * g + 16 * ch, dk);
-        // dSᵀ row r, query columns 64g+32ch .. +31 -> swizzled SMEM block g (the dQ GEMM's A operand)
-        const uint32_t rowaddr = sb + C::OFF_DS + g * C::BLK_BYTES + r * 128;
+        if constexpr (C::DS_IN_DO) {
+          if (ch == 0 && !wait_bounded(bar(C::B_DVDONE), ii & 1, abort_flag, p.err, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t chunk = (ch * 4 + u) ^ (r & 7);
@@ -593,14 +678,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                        : "memory");
         }
       }
-      tmem_wait_st();
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
-      if (ii + 1 < nq) {
-        publish_stat(ii + 1, stat_next);
-        if (ii + 2 < nq) stat_next = load_stat(ii + 2);
-      }
+      if (ii + 1 < nq) publish_stat(ii + 1, stat_next);
+      stat_next = stat_after;
     }
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
