@@ -81,6 +81,27 @@ def test_backward_full_size_sampled(name):
     assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
 
 
+@pytest.mark.slow
+def test_backward_long_first_key_tile():
+    """long_n32768 (B=1, H=8, N=32768, causal): dK and dV of the first key
+    tile (keys 0-127) of one head against the oracle.  These are the heaviest
+    key tiles of the launch: their loop runs all 256 query tiles, wrapping
+    the Q/dO ring and the dQ staging many times, and every query row of the
+    sequence contributes to them (the oracle's cost is the full N x N
+    attention of the head)."""
+    fa = require_gpu()
+    w = wl.WORKLOADS["long_n32768"]
+    q, k, v, do = wl.workload_inputs(w, seed=0)
+    dq, dk, dv = _run(fa, q, k, v, do, w.causal)
+    h = 5
+    one = (slice(None), slice(None), slice(h, h + 1), slice(None))
+    keys = np.arange(128)
+    _, DK, DV = oracle.backward_rows(f64(q[one]), f64(k[one]), f64(v[one]), f64(do[one]), w.scale, w.causal,
+                                     0, 0, [], keys)
+    assert rel_fro(dk[0, keys, h], DK) <= GRAD_RTOL
+    assert rel_fro(dv[0, keys, h], DV) <= GRAD_RTOL
+
+
 def test_backward_repeatable_and_workspace_reuse():
     """dQ is accumulated by unordered reduce-adds: results vary only by rounding order;
     a dirty reused workspace must not leak into the result."""

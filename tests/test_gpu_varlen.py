@@ -58,8 +58,9 @@ def test_varlen_empty_sequence_and_untouched_lse_tail():
 
 def test_varlen16_workload_sampled():
     """The 16-sequence packed workload (lengths uniform in [64, 4096]) at full
-    size; the oracle checks the shortest and longest sequence on two heads,
-    and every sequence's forward on sampled rows."""
+    size; the oracle checks every sequence's forward on sampled rows of one
+    head, every sequence's backward on one head, and the shortest and longest
+    sequence's backward on two more heads."""
     fa = require_gpu()
     w = wl.WORKLOADS["varlen16"]
     cu, q, k, v, do = wl.workload_inputs(w, seed=0)
@@ -77,12 +78,12 @@ def test_varlen16_workload_sampled():
         O, L = oracle.forward_rows(qd[None, a:a + n], kd[None, a:a + n], vd[None, a:a + n], w.scale, True, 0, h, rows)
         assert np.abs(o[a + rows, h] - O).max() <= O_ATOL
         assert np.abs(lse[s, h, rows] - L).max() <= LSE_ATOL
-    for s in (int(np.argmin(lengths)), int(np.argmax(lengths))):
-        a, n = cun[s], lengths[s]
-        for h in (0, w.H - 1):
-            sl = slice(a, a + n)
-            DQ, DK, DV = oracle.backward(qd[None, sl, h:h + 1], kd[None, sl, h:h + 1], vd[None, sl, h:h + 1],
-                                         dod[None, sl, h:h + 1], w.scale, True)
-            assert rel_fro(dq[sl, h], DQ[0, :, 0]) <= GRAD_RTOL
-            assert rel_fro(dk[sl, h], DK[0, :, 0]) <= GRAD_RTOL
-            assert rel_fro(dv[sl, h], DV[0, :, 0]) <= GRAD_RTOL
+    checks = [(s, int(rng.integers(w.H))) for s in range(len(lengths))]
+    checks += [(s, h) for s in (int(np.argmin(lengths)), int(np.argmax(lengths))) for h in (0, w.H - 1)]
+    for s, h in checks:
+        sl = slice(cun[s], cun[s] + lengths[s])
+        DQ, DK, DV = oracle.backward(qd[None, sl, h:h + 1], kd[None, sl, h:h + 1], vd[None, sl, h:h + 1],
+                                     dod[None, sl, h:h + 1], w.scale, True)
+        assert rel_fro(dq[sl, h], DQ[0, :, 0]) <= GRAD_RTOL, (s, h)
+        assert rel_fro(dk[sl, h], DK[0, :, 0]) <= GRAD_RTOL, (s, h)
+        assert rel_fro(dv[sl, h], DV[0, :, 0]) <= GRAD_RTOL, (s, h)

@@ -248,9 +248,15 @@ def test_gradient_invariants(causal):
 # ---------------------------------------------------------------------------
 # a library routine: PyTorch float64 SDPA with autograd
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N,panel", [(50, None), (1100, None), (200, 48)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_matches_torch_sdpa_float64(causal):
-    B, N, H, d = 2, 50, 3, 16
+def test_matches_torch_sdpa_float64(causal, N, panel, monkeypatch):
+    """N = 1100 spans three of the oracle's 512-row panels, and a 48-row panel
+    at N = 200 five: the panel-by-panel accumulation of dK and dV (summed over
+    query rows) is checked against a library that never splits the rows."""
+    if panel is not None:
+        monkeypatch.setattr(oa, "PANEL_ROWS", panel)
+    B, H, d = (2, 3, 16) if N <= 200 else (1, 2, 16)
     q, k, v, do = (_rand(B, N, H, d) for _ in range(4))
     scale = 1.0 / math.sqrt(d)
     O, L = oracle.forward(q, k, v, scale, causal)
