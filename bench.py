@@ -91,8 +91,9 @@ def _cpu_model():
 # ---------------------------------------------------------------------------
 def time_oracle_sample(w: wl.Workload, budget_s: float, seed: int = 0):
     """Run the fp64 oracle forward + backward on whole (batch, head) problems
-    of the workload until `budget_s` has elapsed (at least one).  Returns
-    (TFLOP/s by the workload's FLOP convention, seconds, heads done)."""
+    of the workload, cycling through them, until `budget_s` has elapsed (at
+    least one).  Returns (TFLOP/s by the workload's FLOP convention, seconds,
+    problems done)."""
     import numpy as np
 
     import oracle
@@ -100,7 +101,8 @@ def time_oracle_sample(w: wl.Workload, budget_s: float, seed: int = 0):
     q, k, v, do = wl.workload_inputs(w, seed)
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     done, t0 = 0, time.perf_counter()
-    for b, h in heads:
+    while True:
+        b, h = heads[done % len(heads)]
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
         qd, kd, vd, dod = (t[sl].float().double().numpy() for t in (q, k, v, do))
         oracle.forward(qd, kd, vd, w.scale, w.causal)
@@ -112,6 +114,50 @@ def time_oracle_sample(w: wl.Workload, budget_s: float, seed: int = 0):
     flops = (wl.flops_fwd(1, w.d, [w.N], w.causal) + wl.flops_bwd(1, w.d, [w.N], w.causal)) * done
     del np
     return flops / dt / 1e12, dt, done
+
+
+# Bounded oracle samples of the three smallest dense configurations, for the
+# cpu_baseline record: (workload, seconds of work on all cores, on one core).
+CPU_CONFIG_SAMPLES = (("tiny", 1.0, 1.0), ("small", 2.5, 2.5), ("mid_n4096_d128", 0.0, 3.0))
+
+
+def _cpu_sample_records(names_budgets, cores):
+    out = []
+    for name, budget in names_budgets:
+        w = wl.WORKLOADS[name]
+        v, dt, n = time_oracle_sample(w, budget)
+        out.append({"workload": name, "cores": cores, "value": v, "unit": "TFLOP/s", "seconds": dt,
+                    "sample": f"{n} (batch, head) problem(s) of {w.B * w.H}, fwd+bwd"})
+    return out
+
+
+def cpu_baseline_configs(all_cores: int):
+    """The oracle on the tiny, small and mid configurations, on all host cores
+    (this process; BLAS threads = all cores, numpy's elementwise steps on one)
+    and on one core (a child interpreter pinned to one CPU with one BLAS
+    thread)."""
+    recs = _cpu_sample_records([(n, b) for n, b, _ in CPU_CONFIG_SAMPLES if b > 0], all_cores)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    spec = ",".join(f"{n}:{b1}" for n, _, b1 in CPU_CONFIG_SAMPLES)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-one-core", spec], env=env,
+                           capture_output=True, text=True, timeout=300)
+        recs += json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # the all-cores records stand on their own
+        recs.append({"one_core": f"not measured: {type(e).__name__}"})
+    return recs
+
+
+def run_cpu_one_core(spec: str):
+    """Child side of cpu_baseline_configs: pin this process to one CPU and
+    time the named samples; prints one JSON list."""
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    pairs = [(x.split(":")[0], float(x.split(":")[1])) for x in spec.split(",")]
+    print(json.dumps(_cpu_sample_records(pairs, 1)), flush=True)
+    return 0
 
 
 def run_reference(args, w):
@@ -315,10 +361,18 @@ def run_gpu(args, w):
                          "note": e2e["note"]}
     if rank == 0 and not args.no_cpu_baseline and ws_n == 1:
         v_cpu, dt, heads = time_oracle_sample(w, args.cpu_budget)
+        cores = _host_cores()
         result["cpu_baseline"] = {
-            "value": v_cpu, "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
+            "value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{heads} of {w.B * w.H} (batch, head) problems of {w.name}, fwd+bwd, fp64 numpy oracle, "
-                      f"{dt:.1f} s on {_cpu_model()}"}
+                      f"{dt:.1f} s on {_cpu_model()}",
+            "nproc": os.cpu_count(), "cpu_model": _cpu_model(),
+            "threads_note": "cores = BLAS threads of the matmuls; numpy's elementwise steps (exp, masks) run on one",
+            "configs": cpu_baseline_configs(cores)}
+        if w.name == "mid_n4096_d128":  # the headline sample above is this workload's all-cores record
+            result["cpu_baseline"]["configs"].append({
+                "workload": w.name, "cores": cores, "value": v_cpu, "unit": "TFLOP/s", "seconds": dt,
+                "sample": f"{heads} (batch, head) problem(s) of {w.B * w.H}, fwd+bwd (the headline sample)"})
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws_n > 1:
@@ -532,7 +586,10 @@ def main(argv=None):
                     help="instead of the benchmark: one causal d=128 forward + backward per N (B=1, H=--sweep-bh), "
                          "for a DRAM-counter capture; no N given: 1024 .. 32768")
     ap.add_argument("--sweep-bh", type=int, default=8)
+    ap.add_argument("--cpu-one-core", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.cpu_one_core:
+        return run_cpu_one_core(args.cpu_one_core)
     if args.dram_sweep is not None:
         if not args.dram_sweep:
             args.dram_sweep = [1024, 2048, 4096, 8192, 16384, 32768]
