@@ -76,11 +76,18 @@ def _host_cores():
     return os.cpu_count() or 1
 
 
+# Arm CPU part numbers (/proc/cpuinfo "CPU part", implementer 0x41) of the
+# server cores a GPU machine may have.
+_ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+              "0xd49": "Arm Neoverse N2", "0xd84": "Arm Neoverse V3"}
+
+
 def _cpu_model():
     try:
         for line in open("/proc/cpuinfo"):
             if line.lower().startswith(("model name", "cpu part")):
-                return line.split(":", 1)[1].strip()
+                v = line.split(":", 1)[1].strip()
+                return f"{_ARM_PARTS[v]} (CPU part {v})" if v in _ARM_PARTS else v
     except Exception:
         pass
     return "unknown"
