@@ -241,8 +241,8 @@ FA_API fa_status fa_set_kernel_events(void* start_event, void* end_event);
  * free up.  The items go in groups of `group` consecutive pairs: every tile
  * of a group before the next group; within a group, tile by tile, pairs in
  * order.  `group` is the smallest divisor of npairs whose group·ntiles items
- * fill at least two waves of `slots` resident CTAs (searched up to four
- * times that size), else npairs.  Launch configurations: the forward takes
+ * fill at least one wave of `slots` resident CTAs (searched up to four times
+ * that size), else npairs.  Launch configurations: the forward takes
  * 256 query rows per tile at d = 128 (one CTA per SM) and 128 at d = 64 (two
  * per SM); the backward 128 keys per tile, one CTA per SM.
  *   npairs, ntiles, slots  positive; npairs·ntiles <= 2^31 − 1

@@ -33,15 +33,16 @@ struct SeqView {
 // heaviest-first tile order, then the next group.  The CTAs in flight then
 // share the tiles of a few pairs in L2 (a packed batch with hundreds of
 // pairs would otherwise have nearly every CTA in flight on a pair of its
-// own).  A freed SM takes the next CTA, so starting each group's heavy tiles
-// first keeps the causal load balance as long as the groups are equal and
-// each spans at least two waves of CTAs; a short group, or a last group
+// own, and at long sequences the K/V or Q/dO/dQ rows of all pairs would not
+// fit in L2).  A freed SM takes the next CTA, so starting each group's heavy
+// tiles first keeps the causal load balance as long as the groups are equal
+// and each spans at least one wave of CTAs; a shorter group, or a last group
 // smaller than the others, leaves heavy tiles for the end (greedy schedules
 // of the causal tile costs: 20-30 % longer).  Group size: the smallest
-// divisor of the pair count with at least two waves of tiles (searched up to
+// divisor of the pair count with at least one wave of tiles (searched up to
 // 4x that size); all pairs (plain tile-major order) when there is none.
 inline int pair_group_size(int npairs, int ntiles, int slots) {
-  const long long need = (2LL * slots + ntiles - 1) / ntiles;
+  const long long need = (static_cast<long long>(slots) + ntiles - 1) / ntiles;
   for (long long g = need; g < npairs && g <= 4 * need; ++g)
     if (npairs % g == 0) return static_cast<int>(g);
   return npairs;

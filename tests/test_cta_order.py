@@ -38,7 +38,7 @@ def _makespan(costs, slots, overhead=1.0):
 def test_every_item_launched_once(name, npairs, ntiles, slots):
     group, pair, tile = b.fa_cta_order(npairs, ntiles, slots)
     assert npairs % group == 0
-    assert group == npairs or group * ntiles >= 2 * slots
+    assert group == npairs or group * ntiles >= slots
     assert len(pair) == npairs * ntiles
     seen = np.zeros((npairs, ntiles), dtype=np.int64)
     np.add.at(seen, (pair, tile), 1)
