@@ -201,12 +201,17 @@ struct BwdCfg {
   static constexpr int NUM_COMPUTE = 256;              // warps 0-7: two warpgroups
   static constexpr int NUM_DRAIN = 128;                // warps 10-13: one per TMEM lane quarter
   // Warps 14-15 only complete the fourth warpgroup, so that registers can be
-  // moved per warpgroup: 512 threads launch with 128 registers each; the two
-  // compute warpgroups take REG_COMPUTE, the other two give back to REG_OTHER.
+  // moved per warpgroup: the CTA launches with LAUNCH_REGS registers a thread
+  // (65536 / NUM_THREADS in the allocation's steps of 8: 128); the two
+  // compute warpgroups take REG_COMPUTE, the other two give back to
+  // REG_OTHER.  The increases are served from the registers the CTA launched
+  // with, so the split must fit in them or an increase waits forever.
   static constexpr int NUM_THREADS = 512;
+  static constexpr int LAUNCH_REGS = (65536 / NUM_THREADS) & ~7;
   static constexpr int REG_COMPUTE = 168;
   static constexpr int REG_OTHER = 88;
-  static_assert(256 * REG_COMPUTE + 256 * REG_OTHER <= 65536, "register split exceeds the launch allocation");
+  static_assert(NUM_COMPUTE * REG_COMPUTE + (NUM_THREADS - NUM_COMPUTE) * REG_OTHER <= NUM_THREADS * LAUNCH_REGS,
+                "register split exceeds the CTA's launch allocation");
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int DRAIN_WARP0 = 10;
@@ -729,6 +734,16 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   static SmemLimit smem_limit;
   cudaError_t e = smem_limit.ensure(reinterpret_cast<const void*>(fa_bwd_main_kernel<D>), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  // The compute warpgroups' setmaxnreg increase is served from the registers
+  // the CTA launched with; if the compiler gave the kernel fewer than the
+  // split assumes, the increase would never be granted, so refuse to launch.
+  static const int launch_regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, fa_bwd_main_kernel<D>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  if (launch_regs * C::NUM_THREADS <
+      C::NUM_COMPUTE * C::REG_COMPUTE + (C::NUM_THREADS - C::NUM_COMPUTE) * C::REG_OTHER)
+    return cudaErrorInvalidConfiguration;
   int sms = 0;
   e = current_sm_count(sms);
   if (e != cudaSuccess) return e;
