@@ -530,7 +530,7 @@ FA_API fa_status fa_cta_order(int npairs, int ntiles, int slots, int* group, int
   const long long n = capacity < ctas ? capacity : ctas;
   for (long long b = 0; b < n; ++b) {
     int pr = 0, t = 0;
-    fa::item_of_index(b, g, ntiles, pr, t);  // the kernels' own decode of their block index
+    fa::item_of_index(static_cast<uint32_t>(b), g, ntiles, pr, t);  // the kernels' own decode of their block index
     if (tile) tile[b] = t;
     if (pair) pair[b] = pr;
   }

@@ -69,14 +69,18 @@ inline long long grid_ctas(int npairs, int ntiles, int group) {
 
 // Work item (pair, tile) of linear launch index b under groups of `group`
 // pairs of `ntiles` tiles each; pair >= npairs marks an index of the last,
-// partial group with no work.  The kernels decode their block index with it
-// and fa_cta_order reports the launch order with it on the host.
-__host__ __device__ __forceinline__ void item_of_index(long long b, int group, int ntiles, int& pair, int& tile) {
-  const long long per_group = static_cast<long long>(group) * ntiles;
-  const long long grp = b / per_group;
-  const long long r = b - grp * per_group;
-  tile = static_cast<int>(r / group);
-  pair = static_cast<int>(grp * group + (r - static_cast<long long>(tile) * group));
+// partial group with no work.  The kernels decode their work items with it
+// and fa_cta_order reports the launch order with it on the host.  Launches
+// are limited to 2^31 - 1 items, so 32-bit unsigned arithmetic suffices (a
+// 64-bit division would cost the kernels' lean warps registers).
+__host__ __device__ __forceinline__ void item_of_index(uint32_t b, uint32_t group, uint32_t ntiles, int& pair,
+                                                       int& tile) {
+  const uint32_t per_group = group * ntiles;
+  const uint32_t grp = b / per_group;
+  const uint32_t r = b - grp * per_group;
+  const uint32_t t = r / group;
+  tile = static_cast<int>(t);
+  pair = static_cast<int>(grp * group + (r - t * group));
 }
 
 // (pair, tile) of this CTA.

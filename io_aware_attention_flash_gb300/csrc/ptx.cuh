@@ -264,9 +264,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 
 // The descriptor of an operand `byte_off` bytes further into shared memory
 // (the start-address field holds address / 16 in 14 bits; shared-memory
-// addresses stay below 2^18, so the add does not carry out of the field).
+// addresses stay below 2^18, so the add does not carry out of the field, and
+// a 32-bit add on the low word is exact: one instruction per operand in the
+// MMA thread's issue loop instead of a 64-bit add).
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
-  return desc + static_cast<uint64_t>(byte_off >> 4);
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(desc));
+  lo += byte_off >> 4;
+  uint64_t out;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(out) : "r"(lo), "r"(hi));
+  return out;
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
