@@ -278,6 +278,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
             }
             tc_fence_after();
             issue_pv(t, vs, j > 0);
+            // O_t is final after its last PV: under a causal mask query tile
+            // 0 sees one key tile fewer than tile 1, so its epilogue (and the
+            // egress of its TMA store) overlaps tile 1's last iteration.
+            if (j + 1 == nkv[t]) tc_commit(bar(C::B_ODONE + t));
           }
           if (j + 1 < nkv[t]) {
             issue_s(t, ks1);
@@ -288,11 +292,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
         tc_commit(bar(C::B_VEMPTY + vs));
         if (next) tc_commit(bar(C::B_KEMPTY + ks1));
       }
-      // O_t is final.  (Committing a tile's barrier inside the loop, right
-      // after its last PV, so that its epilogue overlaps the other tile's last
-      // iteration, measured no faster.)
-      if (ok)
-        for (int t = 0; t < NQT; ++t) tc_commit(bar(C::B_ODONE + t));
       // Every MMA issued so far must finish before TMEM is released.
       tc_commit(bar(C::B_DRAIN));
       wait_drain(bar(C::B_DRAIN), 0, p.err, p.timeout_ns);
