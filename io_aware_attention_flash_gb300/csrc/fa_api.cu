@@ -105,16 +105,18 @@ fa_status bind_device(const void* ptr) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // bf16 tensor [outer, rows, H, d] (d innermost) viewed as a 4-D TMA map with a
-// 128-row x 64-column box and 128-byte swizzle.  Rows past `rows` (within one
-// outer index) read as zero.
-fa_status make_map(CUtensorMap* map, const void* ptr, int d, int H, long long rows, int outer) {
+// box_rows x 64-column box (128 rows for loads; 32 for the forward's O, which
+// each warp stores for its own 32 rows) and 128-byte swizzle.  Rows past
+// `rows` (within one outer index) read as zero and are not written.
+fa_status make_map(CUtensorMap* map, const void* ptr, int d, int H, long long rows, int outer,
+                   int box_rows = fa::kTile) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail("cuTensorMapEncodeTiled entry point not found", cudaErrorSymbolNotFound);
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(outer)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                                  static_cast<cuuint64_t>(rows) * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(fa::kTile), 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -188,7 +190,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   FA_TRY(make_map(&tq, q, d, H, rows_per_outer, outer));
   FA_TRY(make_map(&tk, k, d, H, rows_per_outer, outer));
   FA_TRY(make_map(&tv, v, d, H, rows_per_outer, outer));
-  FA_TRY(make_map(&to, o, d, H, rows_per_outer, outer));
+  FA_TRY(make_map(&to, o, d, H, rows_per_outer, outer, 32));
   fa::FwdParams p{};
   p.sv.cu_seqlens = cu;
   p.sv.H = H;

@@ -55,7 +55,7 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
   // barriers: q[NQT], kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], sfull[NQT], pfull[NQT],
-  // odone[NQT], ostaged[NQT], drain
+  // odone[NQT], drain
   static constexpr int B_Q = 0;                         // [NQT]: query tile t landed
   static constexpr int B_KFULL = NQT;
   static constexpr int B_KEMPTY = B_KFULL + NSK;
@@ -64,8 +64,7 @@ struct FwdCfg {
   static constexpr int B_SFULL = B_VEMPTY + NSV;
   static constexpr int B_PFULL = B_SFULL + NQT;
   static constexpr int B_ODONE = B_PFULL + NQT;
-  static constexpr int B_OSTAGED = B_ODONE + NQT;       // O_t staged in shared memory for its TMA store
-  static constexpr int B_DRAIN = B_OSTAGED + NQT;
+  static constexpr int B_DRAIN = B_ODONE + NQT;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -161,7 +160,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
       mbar_init(bar(C::B_SFULL + t), 1);
       mbar_init(bar(C::B_PFULL + t), 128);
       mbar_init(bar(C::B_ODONE + t), 1);
-      mbar_init(bar(C::B_OSTAGED + t), 128);
     }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -413,16 +411,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
       }
       if (ok) ok = wait_bounded(bar(C::B_ODONE + t), 0, abort_flag, p.err, p.timeout_ns);
       if (ok) {
-        // O_t / l, as bf16.  A whole tile (every dense tile: the map clips
-        // rows past N; a packed tile that does not run past its sequence) is
-        // staged in the 128-byte swizzled layout over Q_t, which no MMA reads
-        // any more, and written by one TMA store per 64 columns; a packed tile
-        // that ends inside its sequence's last 128 rows is written row by row
-        // (a box would overwrite the next sequence's rows).
+        // O_t / l, as bf16.  A warp's 32 rows (every dense tile: the map
+        // clips rows past N; in a packed batch, 32 rows that do not run past
+        // their sequence) are staged in the 128-byte swizzled layout over Q_t,
+        // which no MMA reads any more, and written by one TMA store per 64
+        // columns; a packed warp slab that ends inside its sequence is written
+        // row by row (a box would overwrite the next sequence's rows).
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.0f / l : 0.f;
         const bool store = q_row < sp.seqlen;
-        const bool via_tma = !p.sv.cu_seqlens || qt + kTile <= sp.seqlen;
+        const bool via_tma = !p.sv.cu_seqlens || qt + 32 * wq + 32 <= sp.seqlen;
         const uint32_t stage = sb + C::OFF_Q + t * C::TILE_BYTES;
         uint16_t* orow = p.o + (static_cast<size_t>(sp.row_base + q_row) * p.sv.H + sp.h) * D;
 #pragma unroll 1
@@ -461,12 +459,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
           p.lse[(static_cast<size_t>(sp.bs) * p.sv.H + sp.h) * p.sv.lse_stride + q_row] = lse;
         }
         if (via_tma) {
+          // Each warp stores its own 32 rows (a 32-row box whose 1024-byte
+          // swizzle atoms line up with the staged rows), so no thread waits
+          // for the rest of the tile to be staged.
           fence_proxy_async_smem();
-          mbar_arrive(bar(C::B_OSTAGED + t));
-          if (r == 0 && wait_bounded(bar(C::B_OSTAGED + t), 0, abort_flag, p.err, p.timeout_ns)) {
+          __syncwarp();
+          if (lane == 0 && qt + 32 * wq < sp.seqlen) {
 #pragma unroll
             for (int kb = 0; kb < C::KB; ++kb)
-              tma_store_4d(&tmO, stage + kb * C::BLK_BYTES, kb * 64, sp.h, sp.tma_row0 + qt, sp.tma_b);
+              tma_store_4d(&tmO, stage + kb * C::BLK_BYTES + wq * 4096, kb * 64, sp.h, sp.tma_row0 + qt + 32 * wq,
+                           sp.tma_b);
             bulk_commit_group();
             // The stage may be released once the copies have read it; their
             // global writes complete before the grid does.
