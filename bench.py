@@ -321,7 +321,7 @@ def run_gpu(args, w):
         barrier()
         e2e = None
         if not args.no_e2e:
-            e2e = run_e2e(fa, w, dev, stream, (q_h, k_h, v_h, do_h), K, flush)
+            e2e = run_e2e(fa, w, dev, stream, (q_h, k_h, v_h, do_h), K, flush, nbuf=args.e2e_buffers)
     if fa.fa_get_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -447,11 +447,11 @@ def whole_job_tflops(world_size: int, flops_per_rank: float, ms_max: float) -> f
     return world_size * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
-def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
+def run_e2e(fa, w, dev, stream, host_inputs, K, flush, nbuf=2):
     """The same step through the public API with pinned host buffers, as a
     user streaming batches would run it: every step's inputs go host->device
     and its O, LSE, dQ, dK, dV come back, all inside the timed region.  Steps
-    are pipelined over three streams with double-buffered device tensors, so
+    are pipelined over three streams with `nbuf` sets of device tensors, so
     step i+1's upload and step i-1's download overlap step i's kernels.
     Within a step the forward starts once Q, K, V are up (dO uploads under
     it) and O, LSE go down while the backward runs, so neither direction of
@@ -460,20 +460,20 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
     hq, hk, hv, hdo = (t.pin_memory() for t in host_inputs)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     s_in, s_out, s_cmp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
-    dev_in = [tuple(torch.empty_like(t, device=dev) for t in host_inputs) for _ in range(2)]
-    dev_out = [None, None]
+    dev_in = [tuple(torch.empty_like(t, device=dev) for t in host_inputs) for _ in range(nbuf)]
+    dev_out = [None] * nbuf
     host_out = [([torch.empty_like(hq).pin_memory() for _ in range(4)],
-                 torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()) for _ in range(2)]
+                 torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()) for _ in range(nbuf)]
     d2h = sum(t.numel() * t.element_size() for t in host_out[0][0]) + host_out[0][1].numel() * 4
     wsp = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
-    n = K + 2
+    n = K + nbuf
     ev_qkv, ev_in, ev_fwd, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(n)] for _ in range(5))
 
     def one_step(i):
-        b = i % 2
+        b = i % nbuf
         q, k, v, do = dev_in[b]
-        if i >= 2:
-            s_in.wait_event(ev_cmp[i - 2])          # the step that last read these inputs has finished
+        if i >= nbuf:
+            s_in.wait_event(ev_cmp[i - nbuf])       # the step that last read these inputs has finished
         with torch.cuda.stream(s_in):
             for dst, src in ((q, hq), (k, hk), (v, hv)):
                 dst.copy_(src, non_blocking=True)
@@ -481,8 +481,8 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
             do.copy_(hdo, non_blocking=True)
         ev_in[i].record(s_in)
         s_cmp.wait_event(ev_qkv[i])
-        if i >= 2:
-            s_cmp.wait_event(ev_out[i - 2])         # its output buffers have been read back
+        if i >= nbuf:
+            s_cmp.wait_event(ev_out[i - nbuf])      # its output buffers have been read back
         with torch.cuda.stream(s_cmp):
             flush.zero_()
             o, lse = fa.attention_forward(q, k, v, w.causal, stream=s_cmp)
@@ -504,18 +504,18 @@ def run_e2e(fa, w, dev, stream, host_inputs, K, flush):
                 t.record_stream(s_out)
         ev_out[i].record(s_out)
 
-    for i in range(2):                              # warm-up steps
+    for i in range(nbuf):                           # warm-up steps
         one_step(i)
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(s_in)
-    for i in range(2, n):
+    for i in range(nbuf, n):
         one_step(i)
     s_in.wait_event(ev_out[n - 1])
     t1.record(s_in)
     torch.cuda.synchronize(dev)
     return {"ms": t0.elapsed_time(t1) / K, "h2d": h2d, "d2h": d2h,
-            "note": "steps pipelined over 3 streams (upload / kernels / download), double-buffered; "
+            "note": f"steps pipelined over 3 streams (upload / kernels / download), {nbuf} buffer sets; "
                     "forward after Q, K, V are up, O and LSE down during the backward"}
 
 
@@ -587,6 +587,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="device buffer sets the end-to-end pipeline rotates through")
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--dram-sweep", type=int, nargs="*", default=None, metavar="N",
