@@ -105,8 +105,8 @@ fa_status bind_device(const void* ptr) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // bf16 tensor [outer, rows, H, d] (d innermost) viewed as a 4-D TMA map with a
-// box_rows x 64-column box (128 rows for loads; 32 for the forward's O, which
-// each warp stores for its own 32 rows) and 128-byte swizzle.  Rows past
+// box_rows x 64-column box (128 rows for loads; 32 for the outputs O, dK and
+// dV, which each warp stores for its own 32 rows) and 128-byte swizzle.  Rows past
 // `rows` (within one outer index) read as zero and are not written.
 fa_status make_map(CUtensorMap* map, const void* ptr, int d, int H, long long rows, int outer,
                    int box_rows = fa::kTile) {
@@ -252,12 +252,14 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   p.nseq = nseq;
   p.err = err;
   p.timeout_ns = kWaitLimitNs;
-  CUtensorMap tdq;
+  CUtensorMap tdq, tdk, tdv;
   FA_TRY(make_map_dq(&tdq, p.dq_accum, d, H, rows));
+  FA_TRY(make_map(&tdk, dk, d, H, rows_per_outer, outer, 32));
+  FA_TRY(make_map(&tdv, dv, d, H, rows_per_outer, outer, 32));
   cudaEvent_t ev0 = t_main_start, ev1 = t_main_end;
   t_main_start = t_main_end = nullptr;
   const cudaError_t e =
-      fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, max_seqlen, static_cast<cudaStream_t>(stream), ev0, ev1);
+      fa::launch_bwd(d, tq, tk, tv, tdo, tdq, tdk, tdv, p, max_seqlen, static_cast<cudaStream_t>(stream), ev0, ev1);
   return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
 }
 

@@ -228,7 +228,8 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                       const __grid_constant__ CUtensorMap tmDV, const BwdParams p) {
   using C = BwdCfg<D>;
   grid_launch_dependents();  // the dQ conversion may be scheduled; it waits for this grid to finish
   extern __shared__ uint8_t smem_raw[];
@@ -309,6 +310,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmDK);
+    tma_prefetch_desc(&tmDV);
     // In the order the first MMAs need them: K and Q_0 (Sᵀ_0), then V and
     // dO_0 (dPᵀ_0), then the rest of the ring.
     mbar_arrive_expect_tx(bar(C::B_K), C::TILE_BYTES);
@@ -692,33 +695,66 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     }
     if (ok) ok = wait_bounded(bar(C::B_DKDV), 0, abort_flag, p.err, p.timeout_ns);
     if (ok) {
-      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
+      // Warpgroup 0 writes dK (scaled), warpgroup 1 writes dV.  Every MMA
+      // has completed, so the K and V tiles in shared memory are free: each
+      // warp stages its 32 rows there (128-byte swizzled, as they were
+      // loaded) and stores them with one TMA store per 64 columns.  (Plain
+      // stores, each warp instruction touching 32 rows 4 KB apart, took
+      // ≈ 4 µs per CTA for these 64 KB.)  A packed 32-row slab that runs past
+      // its sequence's end is written row by row (a box would overwrite the
+      // next sequence's rows).
       tc_fence_after();
       const float mul = g == 0 ? p.scale : 1.0f;
+      const bool via_tma = !p.sv.cu_seqlens || kv0 + 32 * wq + 32 <= sp.seqlen;
+      const uint32_t stage = sb + (g == 0 ? C::OFF_K : C::OFF_V);
       uint16_t* dst = (g == 0 ? p.dk : p.dv) + (static_cast<size_t>(sp.row_base) + kv_row) * row_stride +
                       static_cast<size_t>(sp.h) * D;
       const uint32_t src = lane_addr + (g == 0 ? C::DK_COL : C::DV_COL);
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v32[32];
-        tmem_ld32(src + ch * 32, v32);
+      for (int cb = 0; cb < D / 64; ++cb) {  // 64 columns (one 128-byte swizzle block) per TMEM round trip
+        uint32_t v[2][32];
+        tmem_ld32(src + cb * 64, v[0]);
+        tmem_ld32(src + cb * 64 + 32, v[1]);
         tmem_wait_ld();
-        reg_fence(v32);
-        if (!row_dead) {
+        reg_fence(v[0]);
+        reg_fence(v[1]);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v32[8 * v4 + 0]) * mul, __uint_as_float(v32[8 * v4 + 1]) * mul);
-            w.y = pack_bf16x2(__uint_as_float(v32[8 * v4 + 2]) * mul, __uint_as_float(v32[8 * v4 + 3]) * mul);
-            w.z = pack_bf16x2(__uint_as_float(v32[8 * v4 + 4]) * mul, __uint_as_float(v32[8 * v4 + 5]) * mul);
-            w.w = pack_bf16x2(__uint_as_float(v32[8 * v4 + 6]) * mul, __uint_as_float(v32[8 * v4 + 7]) * mul);
-            reinterpret_cast<uint4*>(dst + ch * 32)[v4] = w;
+        for (int ch = 0; ch < 4; ++ch) {  // 16 columns (two 16-byte chunks) at a time
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(v[ch / 2][(ch % 2) * 16 + 2 * e]) * mul,
+                               __uint_as_float(v[ch / 2][(ch % 2) * 16 + 2 * e + 1]) * mul);
+          if (via_tma) {
+            const uint32_t rowaddr = stage + cb * C::BLK_BYTES + r * 128;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t chunk = (ch * 2 + u) ^ (r & 7);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowaddr + chunk * 16), "r"(w[4 * u]),
+                           "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                           : "memory");
+            }
+          } else if (!row_dead) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cb * 64 + ch * 16);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
+        }
+      }
+      if (via_tma) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && kv0 + 32 * wq < sp.seqlen) {
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_store_4d(g == 0 ? &tmDK : &tmDV, stage + kb * C::BLK_BYTES + wq * 4096, kb * 64, sp.h,
+                         sp.tma_row0 + kv0 + 32 * wq, sp.tma_b);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the stage may be released once the copies have read it
         }
       }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -729,7 +765,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const CUtensorMap& tdq, const BwdParams& p, int max_seqlen, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
+                         const CUtensorMap& tdq, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                         int max_seqlen, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
   using C = BwdCfg<D>;
   static SmemLimit smem_limit;
   cudaError_t e = smem_limit.ensure(reinterpret_cast<const void*>(fa_bwd_main_kernel<D>), C::SMEM_BYTES);
@@ -764,7 +801,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // before reading what it wrote).  An event recorded between two kernels
   // (timing the main kernel alone) keeps them apart.
   e = launch_kernel(fa_bwd_main_kernel<D>, grid, dim3(C::NUM_THREADS), C::SMEM_BYTES, s, ev0 == nullptr, tq, tk, tv,
-                    tdo, tdq, pm);
+                    tdo, tdq, tdk, tdv, pm);
   if (e != cudaSuccess) return e;
   if (ev1 && (e = cudaEventRecord(ev1, s)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(pairs) * D / 8;
@@ -775,10 +812,11 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdParams& p, int max_seqlen,
                        cudaStream_t s, cudaEvent_t main_start, cudaEvent_t main_end) {
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, max_seqlen, s, main_start, main_end);
-  return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, max_seqlen, s, main_start, main_end);
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, max_seqlen, s, main_start, main_end);
+  return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, max_seqlen, s, main_start, main_end);
 }
 
 }  // namespace fa

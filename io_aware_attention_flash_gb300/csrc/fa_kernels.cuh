@@ -208,7 +208,8 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, int nseq, int max_seqlen, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int max_seqlen,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdParams& p, int max_seqlen,
                        cudaStream_t s,
                        cudaEvent_t main_start = nullptr, cudaEvent_t main_end = nullptr);
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
