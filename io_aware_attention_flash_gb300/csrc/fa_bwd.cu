@@ -208,8 +208,8 @@ struct BwdCfg {
   // with, so the split must fit in them or an increase waits forever.
   static constexpr int NUM_THREADS = 512;
   static constexpr int LAUNCH_REGS = (65536 / NUM_THREADS) & ~7;
-  static constexpr int REG_COMPUTE = 168;
-  static constexpr int REG_OTHER = 88;
+  static constexpr int REG_COMPUTE = 160;
+  static constexpr int REG_OTHER = 96;
   static_assert(NUM_COMPUTE * REG_COMPUTE + (NUM_THREADS - NUM_COMPUTE) * REG_OTHER <= NUM_THREADS * LAUNCH_REGS,
                 "register split exceeds the CTA's launch allocation");
   static constexpr int PRODUCER_WARP = 8;
