@@ -360,6 +360,16 @@ def run_gpu(args, w):
         "gpu_launches": 7 * K,
         "clocks": clocks.summary(),
     }
+    # A second reference: the tensor pipe's own issue rate at the measured
+    # clock (8192 bf16 FLOP per clock per SM for 128x128x16 tcgen05 MMAs, the
+    # rate the MMA-stream microbenchmark sustains), which the cuBLAS-measured
+    # peak above (taken at a lower clock) understates.
+    sm_mhz = result["clocks"].get("sm_mhz")
+    if sm_mhz:
+        mma = 8192 * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6 / 1e12
+        result["mma_rate"] = {"tflops": mma, "basis": "8192 FLOP/clk/SM x SMs x median SM clock",
+                              "fwd_frac": fwd_tflops / mma, "bwd_frac": bwd_tflops / mma,
+                              "bwd_main_kernel_frac": main_tflops / mma}
     if not args.no_decode:
         result["decode"] = run_decode(fa, dev, flush, 20, args.warmup, args.seed + rank, hbm_peak)
     if e2e is not None:

@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
     // before the whole set has landed.
     load_q(0);
     if (preloaded > 0) load_k(0);
+#pragma unroll
     for (int t = 1; t < NQT; ++t)
       if (nkv[t] > 0) load_q(t);
     if (preloaded > 0) load_v(0);
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
       // shared memory corrupts whatever the SM runs next.  On a clean run all
       // of these phases have completed already (the MMA thread waited on
       // them), so the waits return at once.
+#pragma unroll
       for (int t = 0; t < NQT; ++t)
         if (nkv[t] > 0) wait_drain(bar(C::B_Q + t), 0, p.err, p.timeout_ns);
       for (int s = 0; s < C::NSK && s < k_fills; ++s)
@@ -248,13 +250,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
                  (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bounded(bar(C::B_KFULL + 0), 0, abort_flag, p.err, p.timeout_ns);
-      for (int t = 0; ok && t < NQT; ++t) {
-        if (nkv[t] > 0) {
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        if (ok && nkv[t] > 0) {
           ok = wait_bounded(bar(C::B_Q + t), 0, abort_flag, p.err, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(t, 0);
-          tc_commit(bar(C::B_SFULL + t));
+          if (ok) {
+            tc_fence_after();
+            issue_s(t, 0);
+            tc_commit(bar(C::B_SFULL + t));
+          }
         }
       }
       if (ok) tc_commit(bar(C::B_KEMPTY + 0));
@@ -301,7 +305,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
     const int r = wq * 32 + lane;
     const int qt = q0 + t * kTile;
     const int q_row = qt + r;  // row within the sequence
-    if (nkv[t] > 0) {
+    // This warp's tile's key count, computed rather than read from nkv[] with
+    // a run-time index (which would put the array in local memory).
+    const int nkv_t = qt >= sp.seqlen ? 0 : (p.causal ? min(nkv_total, qt / kTile + 1) : nkv_total);
+    if (nkv_t > 0) {
       const float c = p.scale_log2;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
       const uint32_t tS = lane_addr + C::S_COL(t);
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQT_>::NUM_THREADS, FwdCfg<D, NQT_>:
       float m_ref = -CUDART_INF_F;
       float l = 0.f;
       bool ok = true;
-      for (int j = 0; j < nkv[t]; ++j) {
+      for (int j = 0; j < nkv_t; ++j) {
         if (!wait_bounded(bar(C::B_SFULL + t), j & 1, abort_flag, p.err, p.timeout_ns)) {
           ok = false;
           break;
