@@ -60,34 +60,39 @@ __device__ __forceinline__ void locate_row(const SeqView& sv, int nseq, int g, i
 }
 
 // ----------------------------------------------------------------------------
-// fa_bwd_pre: one warp per (row, head).
+// fa_bwd_pre: D/8 threads per (row, head), 16 bytes of O and of dO each (two
+// 16-byte loads in flight per thread, enough to keep HBM busy at one load
+// round trip per thread).
 // ----------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   grid_launch_dependents();  // the main kernel's prologue and first MMAs need nothing from here
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  constexpr int TPR = D / 8;  // threads per (row, head); rows do not straddle warps (TPR divides 32)
+  static_assert(32 % TPR == 0, "a (row, head) lies within one warp");
   const int H = p.sv.H;
-  if (wid >= p.rows * H) return;
-  const int g = wid / H, h = wid - (wid / H) * H;
-  const size_t base = (static_cast<size_t>(g) * H + h) * D;
-  constexpr int E = D / 32;  // elements per lane (2 or 4)
+  const long long total = static_cast<long long>(p.rows) * H;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long rh = tid / TPR;  // (row, head) = row·H + head
+  const int part = static_cast<int>(tid % TPR);
+  const bool live = rh < total;
   float acc = 0.f;
-  if constexpr (E == 4) {
-    const uint2 o = *reinterpret_cast<const uint2*>(p.o + base + lane * 4);
-    const uint2 d = *reinterpret_cast<const uint2*>(p.dout + base + lane * 4);
+  if (live) {
+    const size_t base = static_cast<size_t>(rh) * D + part * 8;  // [rows, H, d] element offset
+    const uint4 o = *reinterpret_cast<const uint4*>(p.o + base);
+    const uint4 d = *reinterpret_cast<const uint4*>(p.dout + base);
     acc = bf16lo_to_f32(o.x) * bf16lo_to_f32(d.x) + bf16hi_to_f32(o.x) * bf16hi_to_f32(d.x) +
-          bf16lo_to_f32(o.y) * bf16lo_to_f32(d.y) + bf16hi_to_f32(o.y) * bf16hi_to_f32(d.y);
-    *reinterpret_cast<float4*>(p.dq_accum + base + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    const uint32_t o = *reinterpret_cast<const uint32_t*>(p.o + base + lane * 2);
-    const uint32_t d = *reinterpret_cast<const uint32_t*>(p.dout + base + lane * 2);
-    acc = bf16lo_to_f32(o) * bf16lo_to_f32(d) + bf16hi_to_f32(o) * bf16hi_to_f32(d);
-    *reinterpret_cast<float2*>(p.dq_accum + base + lane * 2) = make_float2(0.f, 0.f);
+          bf16lo_to_f32(o.y) * bf16lo_to_f32(d.y) + bf16hi_to_f32(o.y) * bf16hi_to_f32(d.y) +
+          bf16lo_to_f32(o.z) * bf16lo_to_f32(d.z) + bf16hi_to_f32(o.z) * bf16hi_to_f32(d.z) +
+          bf16lo_to_f32(o.w) * bf16lo_to_f32(d.w) + bf16hi_to_f32(o.w) * bf16hi_to_f32(d.w);
+    float4* z = reinterpret_cast<float4*>(p.dq_accum + base);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // Every lane takes part in the shuffles (lanes past the end add zeros).
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && part == 0) {
+    const int g = static_cast<int>(rh / H), h = static_cast<int>(rh - (rh / H) * H);
     int bs, local;
     locate_row(p.sv, p.nseq, g, bs, local);
     p.dpsum[(static_cast<size_t>(bs) * H + h) * p.sv.lse_stride + local] = acc;
@@ -792,7 +797,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(ctas));
   const long long pairs = static_cast<long long>(p.rows) * p.sv.H;
-  fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pairs * 32 + 255) / 256), 256, 0, s>>>(p);
+  fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pairs * (D / 8) + 255) / 256), 256, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev0 && (e = cudaEventRecord(ev0, s)) != cudaSuccess) return e;
