@@ -174,3 +174,39 @@ def test_autograd_function():
     assert rel_fro(f64(tq.grad), DQ) <= GRAD_RTOL
     assert rel_fro(f64(tk.grad), DK) <= GRAD_RTOL
     assert rel_fro(f64(tv.grad), DV) <= GRAD_RTOL
+
+
+def test_concurrent_streams_with_separate_workspaces():
+    """Two problems of different shapes (d = 128 causal and d = 64
+    non-causal), each forward and backward on a stream of its own with its
+    own workspace, queued interleaved with no synchronisation: the library's
+    per-device state (shared-memory limits, error word) is shared by both
+    streams, their kernels may overlap on the GPU, and each result must still
+    match the oracle."""
+    fa = require_gpu()
+    from io_aware_attention_flash_gb300 import _binding as bnd
+
+    probs = [(1, 2, 384, 128, True, 31), (2, 3, 200, 64, False, 32)]
+    bufs = []
+    for B, H, N, d, causal, seed in probs:
+        q, k, v, do = wl.make_inputs(B, N, H, d, seed=seed)
+        dev = [t.cuda() for t in (q, k, v, do)]
+        o = torch.empty_like(dev[0])
+        lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+        grads = [torch.empty_like(t) for t in dev[:3]]
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), device="cuda", dtype=torch.uint8)
+        bufs.append(((q, k, v, do), dev, o, lse, grads, ws, causal, d))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for (_, (qc, kc, vc, doc), o, lse, g, ws, causal, d), s in zip(bufs, streams):
+        bnd.fa_fwd(qc, kc, vc, o, lse, causal, stream=s)
+    for (_, (qc, kc, vc, doc), o, lse, g, ws, causal, d), s in zip(bufs, streams):
+        bnd.fa_bwd(qc, kc, vc, o, doc, lse, g[0], g[1], g[2], ws, causal, stream=s)
+    torch.cuda.synchronize()
+    assert_no_device_error(fa)
+    for (q, k, v, do), _, o, lse, g, ws, causal, d in bufs:
+        O, L = oracle.forward(f64(q), f64(k), f64(v), d ** -0.5, causal)
+        assert np.abs(f64(o) - O).max() <= 1e-2
+        DQ, DK, DV = oracle.backward(f64(q), f64(k), f64(v), f64(do), d ** -0.5, causal)
+        for got, ref in zip(g, (DQ, DK, DV)):
+            assert rel_fro(f64(got), ref) <= GRAD_RTOL
